@@ -1,0 +1,170 @@
+/*
+ * pa.h -- C ABI of the paged-attention forward library (GB300, sm_103a).
+ *
+ * The library computes attention over a key/value cache that is stored in
+ * fixed-size physical blocks and reached through a per-sequence block table.
+ * The operations follow these passages:
+ *
+ *   pa_decode        "Perhatian berhalaman" (HF transformers docs), section
+ *                    "Jalur decode": one query token per sequence; the cache
+ *                    is indexed through block_table[batch, max_blocks_per_seq]
+ *                    and updated in place; cache_seqlens gives each
+ *                    sequence's cached length.  "39 · PagedAttention"
+ *                    (inference-notes), sections 1-3: score every key of the
+ *                    sequence in logical order, one softmax, weighted sum of
+ *                    the values; partial results merge with
+ *                    m = max(m1, m2), l = l1 e^(m1-m) + l2 e^(m2-m).
+ *   pa_cache_update  "Perhatian berhalaman", section "Jalur Varlen" ->
+ *                    "Perilaku cache": the varlen kernel cannot reach the
+ *                    paged cache, so the cache is written and read by a
+ *                    separate update step.
+ *   pa_varlen        "Perhatian berhalaman", section "Jalur Varlen" ->
+ *                    "Mekanisme pengindeksan" / "Contoh": packed requests,
+ *                    cumulative lengths cu_seq_lens_q / cu_seq_lens_k,
+ *                    maxima max_length_q / max_length_k.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every pointer argument is DEVICE memory owned by the caller, unless a
+ *    parameter says otherwise.  The library allocates and frees nothing and
+ *    keeps no pointer after a call returns.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream) and never synchronises the host.
+ *  - Tensors are dense and row-major (C order), with the shapes given below.
+ *    q/k/v/out element type is selected by `dtype` and is the same for all of
+ *    them.  Index arrays are int32.
+ *      KV pool  k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim]
+ *      decode   q, out            [batch, num_heads, head_dim]
+ *               k_new, v_new      [batch, num_kv_heads, head_dim]
+ *      varlen   q, out            [total_q, num_heads, head_dim]
+ *               k, v              [total_k, num_kv_heads, head_dim]
+ *  - Query head h reads kv head h / (num_heads / num_kv_heads).
+ *  - softmax_scale <= 0 selects 1 / sqrt(head_dim).
+ *  - Return value: PA_OK, or a negative PA_ERR_* code for misuse the host can
+ *    see (null pointer, unsupported shape or dtype, short workspace).  On a
+ *    negative return nothing was launched and no memory was touched.
+ *  - Problems only the device can see (a needed block_table entry that is
+ *    not a valid block, a length beyond the table, inconsistent cumulative
+ *    lengths) set bits PA_DEVERR_* in *dev_err with an atomic OR, if dev_err
+ *    is not NULL; the affected outputs are written as zeros and no
+ *    out-of-range address is touched.  The kernels never trap and every
+ *    wait inside them is bounded (PA_DEVERR_TIMEOUT).  The caller clears
+ *    *dev_err when it wants to.
+ *
+ * Supported: dtype PA_BF16 or PA_F32; head_dim 64 or 128; for PA_BF16
+ * decode, block_size 16 or 32 and num_heads / num_kv_heads <= 8.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+enum {
+    PA_OK = 0,
+    PA_ERR_NULL = -1,        /* a required pointer is NULL */
+    PA_ERR_DTYPE = -2,       /* dtype not PA_F32 / PA_BF16 */
+    PA_ERR_SHAPE = -3,       /* inconsistent or negative sizes */
+    PA_ERR_UNSUPPORTED = -4, /* valid but not built: head_dim, block_size, group size */
+    PA_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than the query says */
+    PA_ERR_LAUNCH = -6,      /* the CUDA runtime refused a launch or a setup call */
+    PA_ERR_DEVICE = -7       /* no usable CUDA device / not an sm_103 GPU */
+};
+
+/* bits of *dev_err */
+#define PA_DEVERR_BAD_BLOCK 1 /* a needed block_table entry is < 0 or >= num_blocks */
+#define PA_DEVERR_OVERFLOW 2  /* a position lies beyond max_blocks_per_seq * block_size,
+                                 or a length is negative */
+#define PA_DEVERR_BAD_CU 4    /* cu_seq_lens not non-decreasing, or cu_seq_lens_k does not
+                                 equal cache_seqlens + q lengths in pa_cache_update */
+#define PA_DEVERR_TIMEOUT 8   /* a bounded wait inside a kernel gave up */
+
+/*
+ * Bytes of scratch workspace pa_decode needs for these sizes on the current
+ * device (split-K partials and per-sequence merge counters).  0 for PA_F32.
+ */
+size_t pa_decode_workspace_size(int batch, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, pa_dtype dtype);
+
+/*
+ * Decode step: one query per sequence ("Jalur decode").
+ *
+ * For every sequence b, with L = cache_seqlens[b]:
+ *  1. append: k_new[b], v_new[b] are copied bit for bit into the pool at
+ *     logical position L, i.e. physical block block_table[b][L / block_size],
+ *     slot L % block_size (the worked example: 30 -> block 2 slot 30,
+ *     32 -> second block slot 0, 70 -> third block slot 6);
+ *  2. attend: out[b, h] = softmax(q[b, h] . K_j * scale) V_j over the
+ *     L + 1 positions j = 0..L in logical order, the new token included.
+ * cache_seqlens is read only: the caller advances it.  Only the append slot
+ * of each sequence is written in the pool; the caller must not map an
+ * append slot into a block shared with another sequence.
+ *
+ * block_table   [batch, max_blocks_per_seq]; entries past the needed blocks
+ *               may be -1.  The needed blocks are 0 .. L / block_size.
+ * workspace     device scratch of at least pa_decode_workspace_size(...)
+ *               bytes (ignored for PA_F32).  Its contents need not be
+ *               initialised and are not meaningful after the call.  Calls
+ *               that share one workspace must be ordered on the GPU.
+ * Result is independent of where the blocks sit in the pool (bitwise).
+ */
+int pa_decode(const void *q, void *k_cache, void *v_cache, const int32_t *block_table,
+              const int32_t *cache_seqlens, const void *k_new, const void *v_new, void *out,
+              int batch, int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+              int block_size, int max_blocks_per_seq, pa_dtype dtype, float softmax_scale,
+              void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
+
+/*
+ * Varlen cache update ("Jalur Varlen" -> "Perilaku cache").
+ *
+ * k_chunk, v_chunk [total_q, num_kv_heads, head_dim]: the new tokens of all
+ * requests, packed by cu_seq_lens_q [batch + 1].  Row i of request b is
+ * copied bit for bit into the pool at logical position cache_seqlens[b] + i
+ * (cache_seqlens = tokens already cached, read only).
+ *
+ * If k_full, v_full and cu_seq_lens_k are all non-NULL, request b's rows
+ * [cu_seq_lens_k[b], cu_seq_lens_k[b+1]) of k_full/v_full [total_k,
+ * num_kv_heads, head_dim] also receive its whole key sequence in logical
+ * order: the cached prefix read from the pool, then the chunk.  That
+ * requires cu_seq_lens_k[b+1] - cu_seq_lens_k[b] == cache_seqlens[b] +
+ * (cu_seq_lens_q[b+1] - cu_seq_lens_q[b]) (PA_DEVERR_BAD_CU otherwise).
+ * All three NULL: scatter only.  total_k is ignored then.
+ */
+int pa_cache_update(const void *k_chunk, const void *v_chunk, const int32_t *cu_seq_lens_q,
+                    const int32_t *cache_seqlens, const int32_t *block_table, void *k_cache,
+                    void *v_cache, void *k_full, void *v_full, const int32_t *cu_seq_lens_k,
+                    int batch, int total_q, int total_k, int num_kv_heads, int head_dim,
+                    int num_blocks, int block_size, int max_blocks_per_seq, pa_dtype dtype,
+                    int32_t *dev_err, void *stream);
+
+/*
+ * Varlen attention ("Jalur Varlen").  Request r owns q rows
+ * [cu_seq_lens_q[r], cu_seq_lens_q[r+1]) and k/v rows [cu_seq_lens_k[r],
+ * cu_seq_lens_k[r+1]); max_length_q / max_length_k must be at least the
+ * largest q / k length (they size the launch).  causal != 0 masks
+ * bottom-right: query i of a request with lengths (ql, kl) sees key j iff
+ * j <= i + kl - ql.  A query that sees no key gets a zero output row.
+ * PA_BF16 runs on the tcgen05 tensor cores; PA_F32 on CUDA cores.
+ */
+int pa_varlen(const void *q, const void *k, const void *v, const int32_t *cu_seq_lens_q,
+              const int32_t *cu_seq_lens_k, int max_length_q, int max_length_k, int causal,
+              void *out, int batch, int total_q, int total_k, int num_heads, int num_kv_heads,
+              int head_dim, pa_dtype dtype, float softmax_scale, int32_t *dev_err, void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *pa_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

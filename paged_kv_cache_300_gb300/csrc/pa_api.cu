@@ -1,0 +1,253 @@
+// C ABI of the paged-attention library: argument checks, launch planning,
+// TMA descriptor encoding and dispatch.  Every entry point is asynchronous
+// on the caller's stream; nothing here allocates device memory or
+// synchronises the host.
+#include "pa_internal.h"
+
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <mutex>
+
+namespace pa {
+
+int num_sms()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 view of a row-major [rows, heads, head_dim] tensor as
+// (64 dims, heads * head_dim / 64 boxes of 128 bytes, rows); one box is
+// 64 dims x box_rows rows of one head, loaded with 128-byte swizzling.
+int encode_rows_map(CUtensorMap *map, const void *base, uint64_t rows, int heads, int head_dim,
+                    int box_rows)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr) return PA_ERR_DEVICE;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)heads * head_dim / 64, rows};
+    const cuuint64_t strides[2] = {128, (cuuint64_t)heads * head_dim * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_LAUNCH;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+const char *pa_status_string(int status)
+{
+    switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "a required pointer is NULL";
+    case PA_ERR_DTYPE: return "dtype must be PA_F32 or PA_BF16";
+    case PA_ERR_SHAPE: return "inconsistent, negative or misaligned sizes/pointers";
+    case PA_ERR_UNSUPPORTED: return "unsupported head_dim / block_size / group size";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_LAUNCH: return "CUDA launch or setup failed";
+    case PA_ERR_DEVICE: return "no usable CUDA device";
+    default: return "unknown status";
+    }
+}
+
+size_t pa_decode_workspace_size(int batch, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, pa_dtype dtype)
+{
+    if (dtype != PA_BF16 || batch <= 0) return 0;
+    DecodePlan plan;
+    if (decode_bf16_plan(batch, num_heads, num_kv_heads, head_dim, block_size, &plan) != PA_OK)
+        return 0;
+    return decode_workspace_bytes(plan);
+}
+
+int pa_decode(const void *q, void *k_cache, void *v_cache, const int32_t *block_table,
+              const int32_t *cache_seqlens, const void *k_new, const void *v_new, void *out,
+              int batch, int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+              int block_size, int max_blocks_per_seq, pa_dtype dtype, float softmax_scale,
+              void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream)
+{
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
+        block_size <= 0 || max_blocks_per_seq <= 0 || num_heads % num_kv_heads != 0)
+        return PA_ERR_SHAPE;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (batch == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !cache_seqlens || !k_new || !v_new || !out)
+        return PA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) ||
+        !aligned16(v_new) || !aligned16(out))
+        return PA_ERR_SHAPE;
+    if ((long long)num_blocks * block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    DecodeArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.cache_seqlens = cache_seqlens;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.out = out;
+    a.dev_err = dev_err;
+    a.batch = batch;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.num_blocks = num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.group = num_heads / num_kv_heads;
+    a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
+    a.scale_log2 = a.scale * 1.4426950408889634f;
+
+    if (dtype == PA_F32) return decode_f32_launch(a, head_dim, block_size, s);
+
+    DecodePlan plan;
+    int rc = decode_bf16_plan(batch, num_heads, num_kv_heads, head_dim, block_size, &plan);
+    if (rc != PA_OK) return rc;
+    if (workspace == nullptr || workspace_bytes < decode_workspace_bytes(plan) ||
+        !aligned16(workspace))
+        return PA_ERR_WORKSPACE;
+    a.part = static_cast<float *>(workspace);
+    a.tickets = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
+                                            ((plan.part_floats * 4 + 255) & ~(size_t)255));
+    a.head_groups = plan.head_groups;
+    a.nstages = plan.nstages;
+    CUtensorMap tm_k, tm_v;
+    const uint64_t rows = (uint64_t)num_blocks * block_size;
+    if ((rc = encode_rows_map(&tm_k, k_cache, rows, num_kv_heads, head_dim, block_size)) != PA_OK)
+        return rc;
+    if ((rc = encode_rows_map(&tm_v, v_cache, rows, num_kv_heads, head_dim, block_size)) != PA_OK)
+        return rc;
+    if (cudaMemsetAsync(a.tickets, 0, plan.ticket_ints * 4, s) != cudaSuccess) return PA_ERR_LAUNCH;
+    return decode_bf16_launch(a, head_dim, block_size, plan, tm_k, tm_v, s);
+}
+
+int pa_cache_update(const void *k_chunk, const void *v_chunk, const int32_t *cu_seq_lens_q,
+                    const int32_t *cache_seqlens, const int32_t *block_table, void *k_cache,
+                    void *v_cache, void *k_full, void *v_full, const int32_t *cu_seq_lens_k,
+                    int batch, int total_q, int total_k, int num_kv_heads, int head_dim,
+                    int num_blocks, int block_size, int max_blocks_per_seq, pa_dtype dtype,
+                    int32_t *dev_err, void *stream)
+{
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+    const bool gather = k_full != nullptr || v_full != nullptr || cu_seq_lens_k != nullptr;
+    if (batch < 0 || total_q < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
+        block_size <= 0 || max_blocks_per_seq <= 0 || (gather && total_k < 0))
+        return PA_ERR_SHAPE;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (batch == 0) return PA_OK;
+    if (!cu_seq_lens_q || !cache_seqlens || !block_table || !k_cache || !v_cache)
+        return PA_ERR_NULL;
+    if (gather && (!k_full || !v_full || !cu_seq_lens_k)) return PA_ERR_NULL;
+    if (total_q > 0 && (!k_chunk || !v_chunk)) return PA_ERR_NULL;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || (k_chunk && !aligned16(k_chunk)) ||
+        (v_chunk && !aligned16(v_chunk)) || (gather && (!aligned16(k_full) || !aligned16(v_full))))
+        return PA_ERR_SHAPE;
+    CacheUpdateArgs a{};
+    a.k_chunk = k_chunk;
+    a.v_chunk = v_chunk;
+    a.cu_q = cu_seq_lens_q;
+    a.prefix = cache_seqlens;
+    a.block_table = block_table;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.k_full = gather ? k_full : nullptr;
+    a.v_full = gather ? v_full : nullptr;
+    a.cu_k = gather ? cu_seq_lens_k : nullptr;
+    a.dev_err = dev_err;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.total_k = gather ? total_k : 0;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.row_bytes = num_kv_heads * head_dim * (dtype == PA_BF16 ? 2 : 4);
+    return cache_update_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+int pa_varlen(const void *q, const void *k, const void *v, const int32_t *cu_seq_lens_q,
+              const int32_t *cu_seq_lens_k, int max_length_q, int max_length_k, int causal,
+              void *out, int batch, int total_q, int total_k, int num_heads, int num_kv_heads,
+              int head_dim, pa_dtype dtype, float softmax_scale, int32_t *dev_err, void *stream)
+{
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (batch < 0 || total_q < 0 || total_k < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || max_length_q < 0 || max_length_k < 0 || num_heads % num_kv_heads != 0)
+        return PA_ERR_SHAPE;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (batch == 0 || total_q == 0) return PA_OK;
+    if (!q || !out || !cu_seq_lens_q || !cu_seq_lens_k || (total_k > 0 && (!k || !v)))
+        return PA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(out) || (k && !aligned16(k)) || (v && !aligned16(v)))
+        return PA_ERR_SHAPE;
+    VarlenArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.cu_q = cu_seq_lens_q;
+    a.cu_k = cu_seq_lens_k;
+    a.out = out;
+    a.dev_err = dev_err;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.total_k = total_k;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.max_q = max_length_q;
+    a.max_k = max_length_k;
+    a.causal = causal != 0;
+    a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
+    a.scale_log2 = a.scale * 1.4426950408889634f;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == PA_F32) return varlen_f32_launch(a, s);
+    if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+    CUtensorMap tm_q, tm_k, tm_v;
+    int rc;
+    if ((rc = encode_rows_map(&tm_q, q, (uint64_t)total_q, num_heads, head_dim, 128)) != PA_OK)
+        return rc;
+    if (total_k > 0) {
+        if ((rc = encode_rows_map(&tm_k, k, (uint64_t)total_k, num_kv_heads, head_dim, 128)) != PA_OK)
+            return rc;
+        if ((rc = encode_rows_map(&tm_v, v, (uint64_t)total_k, num_kv_heads, head_dim, 128)) != PA_OK)
+            return rc;
+    } else {
+        tm_k = tm_q;
+        tm_v = tm_q;
+    }
+    return varlen_bf16_launch(a, tm_q, tm_k, tm_v, s);
+}
+
+}  // extern "C"

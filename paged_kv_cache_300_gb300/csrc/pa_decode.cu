@@ -1,0 +1,709 @@
+// Paged decode attention (one query per sequence) for GB300.
+//
+// What it computes ("Perhatian berhalaman", HF transformers docs, section
+// "Jalur decode"; "39 · PagedAttention", inference-notes, sections 1-3):
+// for every sequence b the new token's K/V is written in place at logical
+// position L = cache_seqlens[b] (block block_table[b][L / bs], slot L % bs),
+// then the query attends over positions 0..L walked in logical order through
+// the block table: score per key, one softmax, weighted sum of V.
+//
+// bf16 design (HBM-bound):
+//  * Stream-K over the flattened work list.  A "unit" is one logical block
+//    of one sequence for one group of HS kv heads; units are ordered (head
+//    group, sequence, logical block) and the persistent grid of P CTAs takes
+//    equal contiguous ranges, so every SM streams the same number of bytes
+//    whatever the length mix.  Every CTA derives the ranges itself from
+//    cache_seqlens (block-wide scan), so the host needs no lengths and no
+//    device-to-host copy.
+//  * A producer warp resolves logical -> physical blocks through the table
+//    (32 entries per coalesced load) and issues TMA tensor loads of the K and
+//    V tiles of each physical block (one 128-byte-swizzled box per kv head
+//    and 64 dims) into a ring of NST shared-memory stages (mbarrier
+//    full/empty pairs).  KV bytes are read exactly once.
+//  * HS consumer warps, one per kv head.  The GQA group of query heads is
+//    packed into the N=8 side of mma.sync m16n8k16: S^T[token, head] = K q^T
+//    with K straight from swizzled shared memory (ldmatrix), online softmax
+//    in registers (exp2), then O^T[dim, head] += V^T P^T with P moved into
+//    the B layout by movmatrix.  Each KV element is touched once by the
+//    tensor pipe instead of G times by the FMA pipe.
+//  * A sequence split across CTAs leaves partial (acc, m, l) per CTA; the
+//    last CTA to finish it (atomic ticket, no spin) merges the partials in
+//    logical order with m = max(m1, m2), l = l1 e^(m1-m) + l2 e^(m2-m)
+//    (inference-notes, "3. Trên GPU"), the accumulator merged with the same
+//    weights, then normalises.  Merge order depends only on the lengths, so
+//    the output is bitwise independent of the physical block placement.
+//  * The CTA that owns a sequence's last block performs the append: it
+//    copies k_new/v_new into the pool slot and into its staged tile, so the
+//    new token is attended without waiting on its own global write.
+//
+// fp32 path: one warp per (sequence, query head), CUDA-core FMA with expf;
+// kept simple, it serves fp32 inputs (tolerance 1e-5) only.
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+#include <math.h>
+
+namespace pa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int D, int BS, int HS>
+struct Geom {
+    static constexpr int KB = D / 64;                 // 128-byte boxes per head row
+    static constexpr int BOX_BYTES = BS * 128;        // one box: BS rows x 64 dims
+    static constexpr int HEAD_BYTES = KB * BOX_BYTES; // one head's K (or V) tile
+    static constexpr int KV_BYTES = HS * HEAD_BYTES;  // the K (or V) half of a stage
+    static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+    static constexpr int MT = BS / 16; // 16-token m-tiles per block
+    static constexpr int KS = D / 16;  // k-steps of QK^T = 16-dim tiles of PV
+    static constexpr int THREADS = (HS + 1) * 32;
+    static constexpr int NW = HS + 1;
+};
+
+// Position of the walk over units (head group, sequence, logical block).
+struct SeqWalk {
+    int hg, b, j;
+    int nblk; // logical blocks of sequence b (>= 1)
+    int len;  // cache_seqlens[b], or -1 for an invalid length
+    long long sb; // units of sequences 0..b-1 within the head group
+};
+
+__device__ __forceinline__ int seq_blocks(int L, int mbps, int bs, bool *ok)
+{
+    *ok = L >= 0 && (long long)L + 1 <= (long long)mbps * bs;
+    return *ok ? (L + bs) / bs : 1;
+}
+
+__device__ __forceinline__ void walk_load(SeqWalk &w, const int32_t *seqlens, int mbps, int bs)
+{
+    bool ok;
+    int L = __ldg(seqlens + w.b);
+    w.nblk = seq_blocks(L, mbps, bs, &ok);
+    w.len = ok ? L : -1;
+}
+
+__device__ __forceinline__ void walk_next(SeqWalk &w, const int32_t *seqlens, int mbps, int bs,
+                                          int batch)
+{
+    if (++w.j == w.nblk) {
+        w.sb += w.nblk;
+        w.j = 0;
+        if (++w.b == batch) {
+            w.b = 0;
+            w.sb = 0;
+            ++w.hg;
+        }
+        walk_load(w, seqlens, mbps, bs);
+    }
+}
+
+// CTA whose unit range [c U / P, (c+1) U / P) contains unit u.
+__device__ __forceinline__ int cta_of(long long u, int P, long long U)
+{
+    return (int)(((u + 1) * P - 1) / U);
+}
+
+template <int D, int BS, int HS>
+__global__ void __launch_bounds__((HS + 1) * 32, 1)
+    decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a)
+{
+    using Gm = Geom<D, BS, HS>;
+    constexpr int NT = Gm::THREADS, NW = Gm::NW;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int nst = a.nstages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + nst * Gm::STAGE_BYTES);
+    uint64_t *empty = full + nst;
+    int *stage_phys = reinterpret_cast<int *>(empty + nst);
+    __shared__ int s_warp[NW];
+    __shared__ int s_total;
+    __shared__ long long s_start[2]; // first sequence, its unit offset sb
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = a.batch, mbps = a.max_blocks_per_seq;
+    const __nv_bfloat16 *qp = static_cast<const __nv_bfloat16 *>(a.q);
+
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], HS);
+        }
+        fence_mbar_init();
+    }
+    if (warp == HS && lane == 0) {
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+
+    // ---- block-wide exclusive scan of the per-sequence block counts
+    const int per = (B + NT - 1) / NT;
+    const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
+    int local = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+        bool ok;
+        local += seq_blocks(__ldg(a.cache_seqlens + b), mbps, BS, &ok);
+        if (!ok && blockIdx.x == 0) flag_error(a.dev_err, PA_DEVERR_OVERFLOW);
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = lane < NW ? s_warp[lane] : 0;
+        int inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int t = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += t;
+        }
+        if (lane < NW) s_warp[lane] = inc - v;
+        if (lane == NW - 1) s_total = inc;
+    }
+    __syncthreads();
+    const long long ublk = s_total;
+    const long long U = ublk * a.head_groups;
+    const int P = gridDim.x;
+    const long long u0 = (long long)blockIdx.x * U / P;
+    const long long u1 = (long long)(blockIdx.x + 1) * U / P;
+    if (u0 < u1) {
+        const long long r0 = u0 % ublk;
+        long long sb = (long long)s_warp[warp] + incl - local;
+        if (r0 >= sb && r0 < sb + local) {
+            for (int b = b_lo; b < b_hi; ++b) {
+                bool ok;
+                int n = seq_blocks(__ldg(a.cache_seqlens + b), mbps, BS, &ok);
+                if (r0 < sb + n) {
+                    s_start[0] = b;
+                    s_start[1] = sb;
+                    break;
+                }
+                sb += n;
+            }
+        }
+    }
+    __syncthreads();
+    if (u0 >= u1) return;
+
+    SeqWalk w;
+    w.hg = (int)(u0 / ublk);
+    w.b = (int)s_start[0];
+    w.sb = s_start[1];
+    walk_load(w, a.cache_seqlens, mbps, BS);
+    w.j = (int)(u0 % ublk - w.sb);
+
+    if (warp == HS) {
+        // ================= producer: block table -> TMA =================
+        int tab_b = -1, tab_hg = -1, tab_j0 = 0, tab_entry = -1;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (long long u = u0; u < u1; ++u) {
+            if (w.b != tab_b || w.hg != tab_hg || w.j >= tab_j0 + 32) {
+                tab_b = w.b;
+                tab_hg = w.hg;
+                tab_j0 = w.j;
+                const int jj = w.j + lane;
+                tab_entry = (w.len >= 0 && jj < w.nblk)
+                                ? __ldg(a.block_table + (size_t)w.b * mbps + jj)
+                                : -1;
+            }
+            const int p = __shfl_sync(kFull, tab_entry, w.j - tab_j0);
+            const bool valid = w.len >= 0 && p >= 0 && p < a.num_blocks;
+            if (!mbar_wait(&empty[stage], phase ^ 1)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                if (w.len >= 0 && !valid) flag_error(a.dev_err, PA_DEVERR_BAD_BLOCK);
+                stage_phys[stage] = valid ? p : -1;
+                if (valid)
+                    mbar_arrive_expect_tx(&full[stage], Gm::STAGE_BYTES);
+                else
+                    mbar_arrive(&full[stage]);
+            }
+            __syncwarp();
+            if (valid && lane < 2 * HS * Gm::KB) {
+                const int kv = lane / (HS * Gm::KB), rem = lane % (HS * Gm::KB);
+                const int hw = rem / Gm::KB, kb = rem % Gm::KB;
+                const uint32_t dst = smem_u32(smem + stage * Gm::STAGE_BYTES + kv * Gm::KV_BYTES +
+                                              (hw * Gm::KB + kb) * Gm::BOX_BYTES);
+                tma_load_3d(dst, kv ? &tm_v : &tm_k, &full[stage], 0,
+                            (w.hg * HS + hw) * Gm::KB + kb, p * BS);
+            }
+            if (++stage == nst) {
+                stage = 0;
+                phase ^= 1;
+            }
+            walk_next(w, a.cache_seqlens, mbps, BS, B);
+        }
+        if (!ok && lane == 0) flag_error(a.dev_err, PA_DEVERR_TIMEOUT);
+        return;
+    }
+
+    // ================= consumers: one warp per kv head =================
+    const int hw = warp;
+    const int G = a.group;
+    const int Hkv = a.num_kv_heads, Hq = a.num_heads;
+    const int trow = lane >> 2;        // C-fragment row (token / dim) within 8
+    const int g0 = 2 * (lane & 3);     // C-fragment columns g0, g0 + 1 (query heads)
+    const int mi = lane >> 3, mr = lane & 7;
+    const int k_toff = (mi & 1) * 8 + mr, k_doff = (mi >> 1) * 8; // ldmatrix A = K
+    const int v_toff = (mi >> 1) * 8 + mr, v_doff = (mi & 1) * 8; // ldmatrix.trans A = V^T
+    const size_t slot_floats = (size_t)HS * G * (D + 2);
+
+    uint32_t qf[Gm::KS][2];
+    float acc[Gm::KS][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    bool bad = false, open = false;
+    int seg_j0 = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+
+    for (long long u = u0; u < u1; ++u) {
+        const int kvh = w.hg * HS + hw;
+        if (!open) {
+            const int gq = lane >> 2;
+            const __nv_bfloat16 *qrow =
+                qp + ((size_t)w.b * Hq + (size_t)kvh * G + gq) * D + 2 * (lane & 3);
+#pragma unroll
+            for (int ks = 0; ks < Gm::KS; ++ks) {
+                qf[ks][0] = gq < G ? __ldg(reinterpret_cast<const unsigned int *>(qrow + ks * 16)) : 0u;
+                qf[ks][1] =
+                    gq < G ? __ldg(reinterpret_cast<const unsigned int *>(qrow + ks * 16 + 8)) : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < Gm::KS; ++i)
+                acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+            bad = w.len < 0;
+            seg_j0 = w.j;
+            open = true;
+        }
+        if (!mbar_wait(&full[stage], phase)) {
+            if (lane == 0) flag_error(a.dev_err, PA_DEVERR_TIMEOUT);
+            return;
+        }
+        const int p = stage_phys[stage];
+        const int L = w.len;
+        bad |= (p < 0);
+        uint8_t *kst = smem + stage * Gm::STAGE_BYTES + hw * Gm::HEAD_BYTES;
+        uint8_t *vst = kst + Gm::KV_BYTES;
+
+        // in-place append: the block holding position L
+        if (p >= 0 && L >= 0 && w.j == L / BS) {
+            constexpr int EPL = D / 32;
+            const int slot = L % BS, d0 = lane * EPL;
+            const size_t src = ((size_t)w.b * Hkv + kvh) * D + d0;
+            const size_t dst = (((size_t)p * BS + slot) * Hkv + kvh) * D + d0;
+            const uint32_t so = (d0 >> 6) * Gm::BOX_BYTES + sw128_offset(slot, d0 & 63);
+            const __nv_bfloat16 *kn = static_cast<const __nv_bfloat16 *>(a.k_new);
+            const __nv_bfloat16 *vn = static_cast<const __nv_bfloat16 *>(a.v_new);
+            __nv_bfloat16 *kc = static_cast<__nv_bfloat16 *>(a.k_cache);
+            __nv_bfloat16 *vc = static_cast<__nv_bfloat16 *>(a.v_cache);
+            if constexpr (EPL == 4) {
+                const uint2 kx = *reinterpret_cast<const uint2 *>(kn + src);
+                const uint2 vx = *reinterpret_cast<const uint2 *>(vn + src);
+                *reinterpret_cast<uint2 *>(kc + dst) = kx;
+                *reinterpret_cast<uint2 *>(vc + dst) = vx;
+                *reinterpret_cast<uint2 *>(kst + so) = kx;
+                *reinterpret_cast<uint2 *>(vst + so) = vx;
+            } else {
+                const uint32_t kx = *reinterpret_cast<const uint32_t *>(kn + src);
+                const uint32_t vx = *reinterpret_cast<const uint32_t *>(vn + src);
+                *reinterpret_cast<uint32_t *>(kc + dst) = kx;
+                *reinterpret_cast<uint32_t *>(vc + dst) = vx;
+                *reinterpret_cast<uint32_t *>(kst + so) = kx;
+                *reinterpret_cast<uint32_t *>(vst + so) = vx;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // slots past the last position of the sequence: zero their V rows so
+        // that whatever the pool holds there (even NaN) meets a zero weight
+        // as a zero, not as NaN
+        if (p >= 0 && L >= 0 && w.j == w.nblk - 1 && L % BS != BS - 1) {
+            const int r0 = L % BS + 1;
+            const int chunks = (BS - r0) * 8 * Gm::KB;
+            for (int ci = lane; ci < chunks; ci += 32) {
+                const int box = ci / ((BS - r0) * 8), rem = ci % ((BS - r0) * 8);
+                *reinterpret_cast<uint4 *>(vst + box * Gm::BOX_BYTES + (r0 + rem / 8) * 128 +
+                                           (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // ---- S^T[token, head] = K q^T (fp32 accumulators)
+        const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
+        float s[Gm::MT][4];
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt) {
+            s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+            const int t = mt * 16 + k_toff;
+#pragma unroll
+            for (int ks = 0; ks < Gm::KS; ++ks) {
+                const int d = ks * 16 + k_doff;
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(kbase + (d >> 6) * Gm::BOX_BYTES + sw128_offset(t, d & 63), r0, r1, r2, r3);
+                mma_bf16_16816(s[mt], r0, r1, r2, r3, qf[ks][0], qf[ks][1]);
+            }
+        }
+        // ---- mask, scale (log2 domain), online softmax
+        const int pos0 = w.j * BS + trow;
+        float t0 = -INFINITY, t1 = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int pos = pos0 + mt * 16 + ((i >> 1) << 3);
+                const bool vis = p >= 0 && pos <= L;
+                s[mt][i] = vis ? s[mt][i] * a.scale_log2 : -INFINITY;
+                if (i & 1)
+                    t1 = fmaxf(t1, s[mt][i]);
+                else
+                    t0 = fmaxf(t0, s[mt][i]);
+            }
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            t0 = fmaxf(t0, __shfl_xor_sync(kFull, t0, o));
+            t1 = fmaxf(t1, __shfl_xor_sync(kFull, t1, o));
+        }
+        const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = exp2_approx(m0 - mu0), al1 = exp2_approx(m1 - mu1);
+        m0 = mn0;
+        m1 = mn1;
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt) {
+            s[mt][0] = exp2_approx(s[mt][0] - mu0);
+            s[mt][1] = exp2_approx(s[mt][1] - mu1);
+            s[mt][2] = exp2_approx(s[mt][2] - mu0);
+            s[mt][3] = exp2_approx(s[mt][3] - mu1);
+            ps0 += s[mt][0] + s[mt][2];
+            ps1 += s[mt][1] + s[mt][3];
+        }
+        l0 = l0 * al0 + ps0;
+        l1 = l1 * al1 + ps1;
+#pragma unroll
+        for (int dm = 0; dm < Gm::KS; ++dm) {
+            acc[dm][0] *= al0;
+            acc[dm][1] *= al1;
+            acc[dm][2] *= al0;
+            acc[dm][3] *= al1;
+        }
+        // ---- O^T[dim, head] += V^T P^T
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt) {
+            const uint32_t b0 = movmatrix_trans(pack_bf16(s[mt][0], s[mt][1]));
+            const uint32_t b1 = movmatrix_trans(pack_bf16(s[mt][2], s[mt][3]));
+            const int t = mt * 16 + v_toff;
+#pragma unroll
+            for (int dm = 0; dm < Gm::KS; ++dm) {
+                const int d = dm * 16 + v_doff;
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_trans(vbase + (d >> 6) * Gm::BOX_BYTES + sw128_offset(t, d & 63), r0, r1,
+                              r2, r3);
+                mma_bf16_16816(acc[dm], r0, r1, r2, r3, b0, b1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (++stage == nst) {
+            stage = 0;
+            phase ^= 1;
+        }
+
+        // ---- end of this CTA's share of the sequence
+        if (w.j == w.nblk - 1 || u == u1 - 1) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                l0 += __shfl_xor_sync(kFull, l0, o);
+                l1 += __shfl_xor_sync(kFull, l1, o);
+            }
+            __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+            const size_t orow = ((size_t)w.b * Hq + (size_t)kvh * G) * D;
+            if (seg_j0 == 0 && w.j == w.nblk - 1) {
+                // the whole sequence was here: normalise and store
+                const float i0 = (bad || !(l0 > 0.f)) ? 0.f : 1.f / l0;
+                const float i1 = (bad || !(l1 > 0.f)) ? 0.f : 1.f / l1;
+#pragma unroll
+                for (int dm = 0; dm < Gm::KS; ++dm)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int d = dm * 16 + trow + ((i >> 1) << 3), g = g0 + (i & 1);
+                        if (g < G)
+                            out[orow + (size_t)g * D + d] =
+                                __float2bfloat16_rn(acc[dm][i] * ((i & 1) ? i1 : i0));
+                    }
+            } else {
+                // partial (acc, m, l) into slot (CTA + segment row)
+                const long long F = (long long)w.hg * ublk + w.sb;
+                const int cfirst = cta_of(F, P, U), clast = cta_of(F + w.nblk - 1, P, U);
+                const long long segrow = (long long)w.hg * B + w.b;
+                float *slot = a.part + (size_t)(blockIdx.x + segrow) * slot_floats;
+                float *pacc = slot + (size_t)hw * G * D;
+                float *pml = slot + (size_t)HS * G * D + (size_t)hw * G * 2;
+#pragma unroll
+                for (int dm = 0; dm < Gm::KS; ++dm)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int d = dm * 16 + trow + ((i >> 1) << 3), g = g0 + (i & 1);
+                        if (g < G) pacc[(size_t)g * D + d] = acc[dm][i];
+                    }
+                if (trow == 0) {
+                    if (g0 < G) {
+                        pml[g0 * 2] = m0;
+                        pml[g0 * 2 + 1] = bad ? -1.f : l0;
+                    }
+                    if (g0 + 1 < G) {
+                        pml[g0 * 2 + 2] = m1;
+                        pml[g0 * 2 + 3] = bad ? -1.f : l1;
+                    }
+                }
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                int32_t *ticket = a.tickets + (size_t)w.b * Hkv + kvh;
+                if (lane == 0) last = atomicAdd(ticket, 1) == clast - cfirst;
+                last = __shfl_sync(kFull, last, 0);
+                if (last) {
+                    __threadfence();
+                    // fold the partials in logical (CTA) order
+                    for (int g = 0; g < G; ++g) {
+                        float m = -INFINITY, l = 0.f, o[D / 32];
+                        bool anybad = false;
+#pragma unroll
+                        for (int k = 0; k < D / 32; ++k) o[k] = 0.f;
+                        for (int c = cfirst; c <= clast; ++c) {
+                            const float *sc = a.part + (size_t)(c + segrow) * slot_floats;
+                            const float mc = __ldcg(sc + (size_t)HS * G * D + (hw * G + g) * 2);
+                            const float lc = __ldcg(sc + (size_t)HS * G * D + (hw * G + g) * 2 + 1);
+                            anybad |= lc < 0.f;
+                            const float mn = fmaxf(m, mc);
+                            const float mu = mn == -INFINITY ? 0.f : mn;
+                            const float wa = exp2_approx(m - mu), wb = exp2_approx(mc - mu);
+                            l = l * wa + lc * wb;
+                            const float *pc = sc + ((size_t)hw * G + g) * D;
+#pragma unroll
+                            for (int k = 0; k < D / 32; ++k)
+                                o[k] = o[k] * wa + __ldcg(pc + lane + 32 * k) * wb;
+                            m = mn;
+                        }
+                        const float inv = (anybad || !(l > 0.f)) ? 0.f : 1.f / l;
+#pragma unroll
+                        for (int k = 0; k < D / 32; ++k)
+                            out[orow + (size_t)g * D + lane + 32 * k] = __float2bfloat16_rn(o[k] * inv);
+                    }
+                    if (lane == 0) *ticket = 0;
+                }
+            }
+            open = false;
+        }
+        walk_next(w, a.cache_seqlens, mbps, BS, B);
+    }
+}
+
+// ------------------------------------------------------------------ fp32
+template <int D>
+__global__ void __launch_bounds__(128) decode_f32_kernel(const DecodeArgs a, int bs)
+{
+    constexpr int EPL = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * 4 + warp;
+    if (gw >= (long long)a.batch * a.num_heads) return;
+    const int b = (int)(gw / a.num_heads), h = (int)(gw % a.num_heads);
+    const int G = a.group, kvh = h / G, Hkv = a.num_kv_heads;
+    const float *q = static_cast<const float *>(a.q);
+    const float *kc = static_cast<const float *>(a.k_cache);
+    const float *vc = static_cast<const float *>(a.v_cache);
+    const float *kn = static_cast<const float *>(a.k_new);
+    const float *vn = static_cast<const float *>(a.v_new);
+    float *out = static_cast<float *>(a.out) + ((size_t)b * a.num_heads + h) * D + lane * EPL;
+    const int L = a.cache_seqlens[b];
+    const int mbps = a.max_blocks_per_seq;
+    if (L < 0 || (long long)L + 1 > (long long)mbps * bs) {
+        if (lane == 0) flag_error(a.dev_err, PA_DEVERR_OVERFLOW);
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) out[k] = 0.f;
+        return;
+    }
+    float qv[EPL], acc[EPL];
+#pragma unroll
+    for (int k = 0; k < EPL; ++k) {
+        qv[k] = q[((size_t)b * a.num_heads + h) * D + lane * EPL + k];
+        acc[k] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    bool bad = false;
+    int p_app = -1;
+    for (int j = 0; j <= L; ++j) {
+        const int p = a.block_table[(size_t)b * mbps + j / bs];
+        if (p < 0 || p >= a.num_blocks) {
+            bad = true;
+            break;
+        }
+        const float *krow, *vrow;
+        if (j == L) {
+            p_app = p;
+            krow = kn + ((size_t)b * Hkv + kvh) * D;
+            vrow = vn + ((size_t)b * Hkv + kvh) * D;
+        } else {
+            const size_t off = (((size_t)p * bs + j % bs) * Hkv + kvh) * D;
+            krow = kc + off;
+            vrow = vc + off;
+        }
+        float dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) dot = fmaf(qv[k], krow[lane * EPL + k], dot);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
+        const float sc = dot * a.scale;
+        const float mn = fmaxf(m, sc);
+        const float alpha = expf(m - mn), pj = expf(sc - mn);
+        l = l * alpha + pj;
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) acc[k] = acc[k] * alpha + pj * vrow[lane * EPL + k];
+        m = mn;
+    }
+    if (bad) {
+        if (lane == 0) flag_error(a.dev_err, PA_DEVERR_BAD_BLOCK);
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) out[k] = 0.f;
+        return;
+    }
+    if (h % G == 0) { // one warp per kv head performs the append
+        const size_t dst = (((size_t)p_app * bs + L % bs) * Hkv + kvh) * D + lane * EPL;
+        const size_t src = ((size_t)b * Hkv + kvh) * D + lane * EPL;
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) {
+            const_cast<float *>(kc)[dst + k] = kn[src + k];
+            const_cast<float *>(vc)[dst + k] = vn[src + k];
+        }
+    }
+    const float inv = 1.f / l;
+#pragma unroll
+    for (int k = 0; k < EPL; ++k) out[k] = acc[k] * inv;
+}
+
+template <int D, int BS, int HS>
+int launch_bf16(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &tm_k,
+                const CUtensorMap &tm_v, cudaStream_t s)
+{
+    auto kern = decode_bf16_kernel<D, BS, HS>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)plan.smem_bytes) != cudaSuccess)
+        return PA_ERR_LAUNCH;
+    kern<<<plan.ctas, Geom<D, BS, HS>::THREADS, plan.smem_bytes, s>>>(tm_k, tm_v, a);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+}
+
+template <int D, int BS, int HS>
+int occupancy_of(size_t smem)
+{
+    auto kern = decode_bf16_kernel<D, BS, HS>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Geom<D, BS, HS>::THREADS, smem) !=
+        cudaSuccess)
+        return 0;
+    return n;
+}
+
+}  // namespace
+
+#define PA_DECODE_SWITCH(D_, BS_, HS_, ...)                                                  \
+    do {                                                                                      \
+        if (D_ == 128 && BS_ == 16) {                                                         \
+            if (HS_ == 8) { constexpr int D = 128, BS = 16, HS = 8; __VA_ARGS__; }                   \
+            if (HS_ == 4) { constexpr int D = 128, BS = 16, HS = 4; __VA_ARGS__; }                   \
+            if (HS_ == 2) { constexpr int D = 128, BS = 16, HS = 2; __VA_ARGS__; }                   \
+            if (HS_ == 1) { constexpr int D = 128, BS = 16, HS = 1; __VA_ARGS__; }                   \
+        } else if (D_ == 128 && BS_ == 32) {                                                  \
+            if (HS_ == 8) { constexpr int D = 128, BS = 32, HS = 8; __VA_ARGS__; }                   \
+            if (HS_ == 4) { constexpr int D = 128, BS = 32, HS = 4; __VA_ARGS__; }                   \
+            if (HS_ == 2) { constexpr int D = 128, BS = 32, HS = 2; __VA_ARGS__; }                   \
+            if (HS_ == 1) { constexpr int D = 128, BS = 32, HS = 1; __VA_ARGS__; }                   \
+        } else if (D_ == 64 && BS_ == 16) {                                                   \
+            if (HS_ == 8) { constexpr int D = 64, BS = 16, HS = 8; __VA_ARGS__; }                    \
+            if (HS_ == 4) { constexpr int D = 64, BS = 16, HS = 4; __VA_ARGS__; }                    \
+            if (HS_ == 2) { constexpr int D = 64, BS = 16, HS = 2; __VA_ARGS__; }                    \
+            if (HS_ == 1) { constexpr int D = 64, BS = 16, HS = 1; __VA_ARGS__; }                    \
+        } else if (D_ == 64 && BS_ == 32) {                                                   \
+            if (HS_ == 8) { constexpr int D = 64, BS = 32, HS = 8; __VA_ARGS__; }                    \
+            if (HS_ == 4) { constexpr int D = 64, BS = 32, HS = 4; __VA_ARGS__; }                    \
+            if (HS_ == 2) { constexpr int D = 64, BS = 32, HS = 2; __VA_ARGS__; }                    \
+            if (HS_ == 1) { constexpr int D = 64, BS = 32, HS = 1; __VA_ARGS__; }                    \
+        }                                                                                     \
+    } while (0)
+
+int decode_bf16_plan(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                     DecodePlan *plan)
+{
+    if (!((head_dim == 64 || head_dim == 128) && (block_size == 16 || block_size == 32)))
+        return PA_ERR_UNSUPPORTED;
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
+    const int G = num_heads / num_kv_heads;
+    if (G > 8) return PA_ERR_UNSUPPORTED;
+    int hs = 8;
+    while (num_kv_heads % hs != 0) hs >>= 1;
+    const size_t stage = (size_t)2 * hs * head_dim * block_size * 2;
+    int nst = (int)(196608 / stage);
+    nst = nst < 2 ? 2 : (nst > 8 ? 8 : nst);
+    plan->heads_per_cta = hs;
+    plan->head_groups = num_kv_heads / hs;
+    plan->nstages = nst;
+    plan->smem_bytes = nst * stage + 1024 + (size_t)nst * 20 + 64;
+    int occ = 0;
+    PA_DECODE_SWITCH(head_dim, block_size, hs, { occ = occupancy_of<D, BS, HS>(plan->smem_bytes); });
+    if (occ <= 0) return PA_ERR_LAUNCH;
+    const int sms = num_sms();
+    if (sms <= 0) return PA_ERR_DEVICE;
+    plan->ctas = sms * occ;
+    plan->part_floats = ((size_t)plan->ctas + (size_t)plan->head_groups * batch) *
+                        (size_t)hs * G * (head_dim + 2);
+    plan->ticket_ints = (size_t)batch * num_kv_heads;
+    return PA_OK;
+}
+
+size_t decode_workspace_bytes(const DecodePlan &plan)
+{
+    const size_t part = (plan.part_floats * 4 + 255) & ~(size_t)255;
+    return part + plan.ticket_ints * 4;
+}
+
+int decode_bf16_launch(const DecodeArgs &a, int head_dim, int block_size, const DecodePlan &plan,
+                       const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t s)
+{
+    int rc = PA_ERR_UNSUPPORTED;
+    PA_DECODE_SWITCH(head_dim, block_size, plan.heads_per_cta,
+                     { rc = launch_bf16<D, BS, HS>(a, plan, tm_k, tm_v, s); });
+    return rc;
+}
+
+int decode_f32_launch(const DecodeArgs &a, int head_dim, int block_size, cudaStream_t s)
+{
+    const long long warps = (long long)a.batch * a.num_heads;
+    const unsigned grid = (unsigned)((warps + 3) / 4);
+    if (head_dim == 64)
+        decode_f32_kernel<64><<<grid, 128, 0, s>>>(a, block_size);
+    else if (head_dim == 128)
+        decode_f32_kernel<128><<<grid, 128, 0, s>>>(a, block_size);
+    else
+        return PA_ERR_UNSUPPORTED;
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+}
+
+}  // namespace pa

@@ -1,0 +1,92 @@
+// Host-side interface between the C ABI (pa_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// ------------------------------------------------------------------ decode
+struct DecodeArgs {
+    const void *q;
+    void *k_cache;
+    void *v_cache;
+    const int32_t *block_table;
+    const int32_t *cache_seqlens;
+    const void *k_new;
+    const void *v_new;
+    void *out;
+    float *part;      // split-K partials (bf16 path)
+    int32_t *tickets; // per (sequence, kv head) arrival counters (bf16 path)
+    int32_t *dev_err;
+    int batch, num_heads, num_kv_heads, num_blocks, max_blocks_per_seq;
+    int group;       // num_heads / num_kv_heads
+    int head_groups; // num_kv_heads / kv heads per CTA
+    int nstages;
+    float scale;      // softmax scale
+    float scale_log2; // softmax scale * log2(e)
+};
+
+// Launch geometry of the bf16 decode kernel for one problem shape.
+struct DecodePlan {
+    int heads_per_cta; // kv heads handled by one CTA (one consumer warp each)
+    int head_groups;
+    int nstages;
+    int ctas;          // persistent grid size (stream-K partitions)
+    size_t smem_bytes;
+    size_t part_floats; // partial buffer size in floats
+    size_t ticket_ints;
+};
+
+int decode_bf16_plan(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                     DecodePlan *plan);
+size_t decode_workspace_bytes(const DecodePlan &plan);
+int decode_bf16_launch(const DecodeArgs &a, int head_dim, int block_size, const DecodePlan &plan,
+                       const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t s);
+int decode_f32_launch(const DecodeArgs &a, int head_dim, int block_size, cudaStream_t s);
+
+// ------------------------------------------------------------------ cache update
+struct CacheUpdateArgs {
+    const void *k_chunk;
+    const void *v_chunk;
+    const int32_t *cu_q;
+    const int32_t *prefix;
+    const int32_t *block_table;
+    void *k_cache;
+    void *v_cache;
+    void *k_full;
+    void *v_full;
+    const int32_t *cu_k;
+    int32_t *dev_err;
+    int batch, total_q, total_k, num_kv_heads, head_dim, num_blocks, block_size,
+        max_blocks_per_seq;
+    int row_bytes; // num_kv_heads * head_dim * element size
+};
+int cache_update_launch(const CacheUpdateArgs &a, cudaStream_t s);
+
+// ------------------------------------------------------------------ varlen
+struct VarlenArgs {
+    const void *q;
+    const void *k;
+    const void *v;
+    const int32_t *cu_q;
+    const int32_t *cu_k;
+    void *out;
+    int32_t *dev_err;
+    int batch, total_q, total_k, num_heads, num_kv_heads, head_dim, max_q, max_k, causal;
+    float scale, scale_log2;
+};
+int varlen_f32_launch(const VarlenArgs &a, cudaStream_t s);
+int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                       const CUtensorMap &tm_v, cudaStream_t s);
+
+// ------------------------------------------------------------------ helpers
+int num_sms();
+int encode_rows_map(CUtensorMap *map, const void *base, uint64_t rows, int heads, int head_dim,
+                    int box_rows);
+
+}  // namespace pa
