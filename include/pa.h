@@ -109,9 +109,14 @@ size_t pa_decode_workspace_size(int batch, int num_heads, int num_kv_heads, int 
  * block_table   [batch, max_blocks_per_seq]; entries past the needed blocks
  *               may be -1.  The needed blocks are 0 .. L / block_size.
  * workspace     device scratch of at least pa_decode_workspace_size(...)
- *               bytes (ignored for PA_F32).  Its contents need not be
- *               initialised and are not meaningful after the call.  Calls
- *               that share one workspace must be ordered on the GPU.
+ *               bytes (ignored for PA_F32), 16-byte aligned.  It must be
+ *               zero-filled before its first use; every call leaves it in a
+ *               state the next call accepts (its merge counters back at
+ *               zero, whatever the sizes of the call), so one zero fill at
+ *               allocation is enough.  After a call that reported
+ *               PA_DEVERR_TIMEOUT, zero it again.  Calls that share one
+ *               workspace must be ordered on the GPU.  batch * num_kv_heads
+ *               may not exceed 262144 (PA_ERR_UNSUPPORTED).
  * Result is independent of where the blocks sit in the pool (bitwise).
  */
 int pa_decode(const void *q, void *k_cache, void *v_cache, const int32_t *block_table,

@@ -139,7 +139,7 @@ def _workspace(dev, nbytes):
     key = (dev.index, torch.cuda.current_stream(dev).cuda_stream)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)  # zero on first use
         _workspaces[key] = ws
     return ws
 

@@ -137,9 +137,8 @@ int pa_decode(const void *q, void *k_cache, void *v_cache, const int32_t *block_
     if (workspace == nullptr || workspace_bytes < decode_workspace_bytes(plan) ||
         !aligned16(workspace))
         return PA_ERR_WORKSPACE;
-    a.part = static_cast<float *>(workspace);
-    a.tickets = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
-                                            ((plan.part_floats * 4 + 255) & ~(size_t)255));
+    a.tickets = static_cast<int32_t *>(workspace);
+    a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kTicketRegionBytes);
     a.head_groups = plan.head_groups;
     a.nstages = plan.nstages;
     CUtensorMap tm_k, tm_v;
@@ -148,7 +147,6 @@ int pa_decode(const void *q, void *k_cache, void *v_cache, const int32_t *block_
         return rc;
     if ((rc = encode_rows_map(&tm_v, v_cache, rows, num_kv_heads, head_dim, block_size)) != PA_OK)
         return rc;
-    if (cudaMemsetAsync(a.tickets, 0, plan.ticket_ints * 4, s) != cudaSuccess) return PA_ERR_LAUNCH;
     return decode_bf16_launch(a, head_dim, block_size, plan, tm_k, tm_v, s);
 }
 

@@ -475,7 +475,12 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
                 __syncwarp();
                 int last = 0;
                 int32_t *ticket = a.tickets + (size_t)w.b * Hkv + kvh;
-                if (lane == 0) last = atomicAdd(ticket, 1) == clast - cfirst;
+                // segments of this sequence: every CTA in [cfirst, clast] has units
+                // when U >= P; when U < P a CTA holds at most one unit, so the
+                // sequence has exactly nblk segments, one per unit
+                const bool dense = U >= P;
+                const int nseg = dense ? clast - cfirst + 1 : w.nblk;
+                if (lane == 0) last = atomicAdd(ticket, 1) == nseg - 1;
                 last = __shfl_sync(kFull, last, 0);
                 if (last) {
                     __threadfence();
@@ -485,7 +490,8 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
                         bool anybad = false;
 #pragma unroll
                         for (int k = 0; k < D / 32; ++k) o[k] = 0.f;
-                        for (int c = cfirst; c <= clast; ++c) {
+                        for (int k = 0; k < nseg; ++k) {
+                            const int c = dense ? cfirst + k : cta_of(F + k, P, U);
                             const float *sc = a.part + (size_t)(c + segrow) * slot_floats;
                             const float mc = __ldcg(sc + (size_t)HS * G * D + (hw * G + g) * 2);
                             const float lc = __ldcg(sc + (size_t)HS * G * D + (hw * G + g) * 2 + 1);
@@ -675,13 +681,13 @@ int decode_bf16_plan(int batch, int num_heads, int num_kv_heads, int head_dim, i
     plan->part_floats = ((size_t)plan->ctas + (size_t)plan->head_groups * batch) *
                         (size_t)hs * G * (head_dim + 2);
     plan->ticket_ints = (size_t)batch * num_kv_heads;
+    if (plan->ticket_ints * 4 > kTicketRegionBytes) return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
 
 size_t decode_workspace_bytes(const DecodePlan &plan)
 {
-    const size_t part = (plan.part_floats * 4 + 255) & ~(size_t)255;
-    return part + plan.ticket_ints * 4;
+    return kTicketRegionBytes + plan.part_floats * 4;
 }
 
 int decode_bf16_launch(const DecodeArgs &a, int head_dim, int block_size, const DecodePlan &plan,

@@ -42,6 +42,12 @@ struct DecodePlan {
     size_t ticket_ints;
 };
 
+// The decode workspace starts with a fixed-size region of merge counters
+// (one int per sequence and kv head).  Only counter operations ever touch it
+// and every call leaves its counters at zero, so a workspace zero-filled once
+// stays valid for calls of any shape; the split-K partials follow it.
+constexpr size_t kTicketRegionBytes = size_t(1) << 20;
+
 int decode_bf16_plan(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
                      DecodePlan *plan);
 size_t decode_workspace_bytes(const DecodePlan &plan);
