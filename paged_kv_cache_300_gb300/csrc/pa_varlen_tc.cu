@@ -1,13 +1,355 @@
-// bf16 varlen attention on tcgen05 tensor cores (in progress).
+// bf16 varlen attention on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// What it computes: "Perhatian berhalaman" (HF transformers docs), section
+// "Jalur Varlen": packed requests located by cu_seq_lens_q / cu_seq_lens_k;
+// query i of request r (lengths ql, kl) attends key j (j <= i + kl - ql when
+// causal), softmax(q k^T * scale) v; a query with no visible key gives 0.
+//
+// One CTA per (query head, 128-row query tile, request); grid.x runs over the
+// heads so the CTAs of one GQA group, which read the same K/V tiles, run
+// side by side and share them through L2.  Query tiles are issued from the
+// last (most keys under the causal mask) to the first.
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax: thread r owns query row r of the tile, which is TMEM
+//              lane r.  It reads its row of S from TMEM, masks, keeps the
+//              running max/sum in registers (exp2 domain), writes P (bf16)
+//              into shared memory in the 128-byte-swizzled K-major layout the
+//              tensor core reads, rescales its row of O in TMEM when the
+//              running max grew by more than 2^8 (lazy rescale: P is then
+//              computed against a max up to 8 below the true one, which the
+//              final division by the same running sum cancels exactly), and
+//              in the end divides O by the sum and stores the row.
+//   warp 4     TMA producer: the Q tile once, then K and V tiles of 128 keys
+//              (two 64-dim swizzled boxes each) into a 2-stage ring.
+//   warp 5     TMEM allocator and MMA issuer (one thread): S_j = Q K_j^T into
+//              one of two TMEM S buffers (M=128, N=128, K=16 per instruction,
+//              both operands K-major), then O += P_j V_j with V read MN-major
+//              straight from its TMA tile; tcgen05.commit signals mbarriers.
+// S_{j+1} is computed while the softmax warps work on S_j.
+//
+// TMEM: columns [0,128) and [128,256) hold the two S buffers, [256,384) O.
+// Every mbarrier wait is bounded; on timeout the kernel flags
+// PA_DEVERR_TIMEOUT, frees its TMEM and returns.
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
-namespace pa {
+#include <math.h>
 
-int varlen_bf16_launch(const VarlenArgs &, const CUtensorMap &, const CUtensorMap &,
-                       const CUtensorMap &, cudaStream_t)
+namespace pa {
+namespace {
+
+constexpr int BM = 128;                  // query rows per tile (TMEM lanes)
+constexpr int BN = 128;                  // keys per tile
+constexpr int HD = 128;                  // head_dim
+constexpr int BOX_BYTES = 128 * 128;     // 128 rows x 64 dims bf16, 128-byte swizzled
+constexpr int TILE_BYTES = 2 * BOX_BYTES; // 128 rows x 128 dims
+constexpr int NSTAGE = 2;
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + TILE_BYTES;
+constexpr int OFF_V = OFF_K + NSTAGE * TILE_BYTES;
+constexpr int OFF_P = OFF_V + NSTAGE * TILE_BYTES;
+constexpr int OFF_BAR = OFF_P + TILE_BYTES;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024; // + alignment slack
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_O = 256;
+constexpr float kRescaleThreshold = 8.0f; // log2 units
+
+struct Barriers {
+    uint64_t q_full;
+    uint64_t k_full[NSTAGE];
+    uint64_t v_full[NSTAGE];
+    uint64_t kv_empty[NSTAGE];
+    uint64_t s_full[2];
+    uint64_t p_full;
+    uint64_t o_done;
+    uint32_t tmem_base;
+};
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk)
 {
-    return PA_ERR_UNSUPPORTED;
+    // kk-th 16-element slice of K inside a [128 rows][128] K-major tile made
+    // of two 64-element boxes: box kk / 4, 32 bytes per slice inside a row.
+    return umma_desc_sw128(tile + (uint32_t)(kk >> 2) * BOX_BYTES + (uint32_t)(kk & 3) * 32u, 16u,
+                           1024u);
+}
+
+__device__ __forceinline__ uint64_t v_desc(uint32_t tile, int kk)
+{
+    // V tile [128 keys][128 dims] read as the MN-major B operand (N = dims):
+    // 16 keys per instruction = two 8-row groups (SBO 1024 B); the second
+    // 64-dim box is LBO = 16 KB away.
+    return umma_desc_sw128(tile + (uint32_t)kk * 2048u, (uint32_t)BOX_BYTES, 1024u);
+}
+
+}  // namespace
+}  // namespace pa
+
+namespace pa {
+namespace {
+
+__global__ void __launch_bounds__(THREADS, 1)
+    varlen_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const VarlenArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Barriers *bar = reinterpret_cast<Barriers *>(smem + OFF_BAR);
+    const uint32_t sbase = smem_u32(smem);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, b = blockIdx.z;
+    const int m = gridDim.y - 1 - blockIdx.y; // heavy (late) tiles first
+    const int G = a.num_heads / a.num_kv_heads, kvh = h / G;
+
+    const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
+    const int k0 = __ldg(a.cu_k + b), k1 = __ldg(a.cu_k + b + 1);
+    if (q0 < 0 || q1 < q0 || q1 > a.total_q || k0 < 0 || k1 < k0 || k1 > a.total_k ||
+        q1 - q0 > (int)gridDim.y * BM) {
+        if (tid == 0 && h == 0 && m == 0) flag_error(a.dev_err, PA_DEVERR_BAD_CU);
+        return;
+    }
+    const int ql = q1 - q0, kl = k1 - k0;
+    if (m * BM >= ql) return;
+    const int rows_here = min(BM, ql - m * BM);
+    int n_keys = kl;
+    if (a.causal) n_keys = max(0, min(kl, m * BM + rows_here - 1 + kl - ql + 1));
+    const int n_tiles = (n_keys + BN - 1) / BN;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+
+    if (n_tiles == 0) { // no visible key for any row of the tile
+        if (tid < rows_here) {
+            uint4 *o = reinterpret_cast<uint4 *>(out + ((size_t)(q0 + m * BM + tid) * a.num_heads + h) * HD);
+#pragma unroll
+            for (int c = 0; c < HD / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        mbar_init(&bar->q_full, 1);
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&bar->k_full[s], 1);
+            mbar_init(&bar->v_full[s], 1);
+            mbar_init(&bar->kv_empty[s], 1);
+        }
+        mbar_init(&bar->s_full[0], 1);
+        mbar_init(&bar->s_full[1], 1);
+        mbar_init(&bar->p_full, 4);
+        mbar_init(&bar->o_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(&bar->tmem_base, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar->tmem_base;
+    bool ok = true;
+
+    if (warp == 4) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(&bar->q_full, TILE_BYTES);
+            for (int c = 0; c < 2; ++c)
+                tma_load_3d(sbase + OFF_Q + c * BOX_BYTES, &tm_q, &bar->q_full, 0, h * 2 + c,
+                            q0 + m * BM);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int st = j & 1;
+                if (j >= NSTAGE && !mbar_wait(&bar->kv_empty[st], ((j >> 1) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const int row = k0 + j * BN;
+                mbar_arrive_expect_tx(&bar->k_full[st], TILE_BYTES);
+                for (int c = 0; c < 2; ++c)
+                    tma_load_3d(sbase + OFF_K + st * TILE_BYTES + c * BOX_BYTES, &tm_k,
+                                &bar->k_full[st], 0, kvh * 2 + c, row);
+                mbar_arrive_expect_tx(&bar->v_full[st], TILE_BYTES);
+                for (int c = 0; c < 2; ++c)
+                    tma_load_3d(sbase + OFF_V + st * TILE_BYTES + c * BOX_BYTES, &tm_v,
+                                &bar->v_full[st], 0, kvh * 2 + c, row);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, 0, 0);
+            constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, HD, 0, 1);
+            const uint32_t qs = sbase + OFF_Q, ps = sbase + OFF_P;
+            ok = mbar_wait(&bar->q_full, 0);
+            auto issue_qk = [&](int j) -> bool {
+                const int st = j & 1;
+                if (!mbar_wait(&bar->k_full[st], (j >> 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t ks = sbase + OFF_K + st * TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk)
+                    umma_bf16(tmem + st * BN, kmajor_desc(qs, kk), kmajor_desc(ks, kk), idesc_qk,
+                              kk > 0);
+                umma_commit(&bar->s_full[st]);
+                return true;
+            };
+            if (ok) ok = issue_qk(0);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int st = j & 1;
+                if (j + 1 < n_tiles && !(ok = issue_qk(j + 1))) break;
+                if (!mbar_wait(&bar->p_full, j & 1) || !mbar_wait(&bar->v_full[st], (j >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t vs = sbase + OFF_V + st * TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_bf16(tmem + COL_O, kmajor_desc(ps, kk), v_desc(vs, kk), idesc_pv,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bar->o_done);
+                umma_commit(&bar->kv_empty[st]);
+            }
+            // the producer never waits for the last two stage releases: wait
+            // here so that no commit arrives after the CTA has left
+            for (int t = max(0, n_tiles - 2); t < n_tiles && ok; ++t)
+                ok = mbar_wait(&bar->kv_empty[t & 1], (t >> 1) & 1);
+        }
+        __syncwarp();
+    } else {
+        // ================= softmax: thread r <-> query row r =================
+        const int r = tid;
+        const int i = m * BM + r; // row inside the request
+        const int lim = a.causal ? min(i + kl - ql, kl - 1) : kl - 1; // last visible key
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        const float sl2 = a.scale_log2;
+        float m_run = -INFINITY, l_run = 0.f;
+        uint8_t *prow0 = smem + OFF_P + r * 128;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j & 1;
+            if (!mbar_wait(&bar->s_full[st], (j >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c)
+                tmem_ld32(trow + st * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+            tmem_ld_wait();
+            const int kb = j * BN;
+            float mx = -INFINITY;
+            if (kb + BN - 1 <= lim) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    if (kb + c > lim) s[c] = -INFINITY;
+                    mx = fmaxf(mx, s[c]);
+                }
+            }
+            const float m_new = fmaxf(m_run, mx * sl2);
+            const bool need = m_new > m_run + kRescaleThreshold;
+            float alpha = 1.f;
+            if (need) {
+                alpha = exp2_approx(m_run - m_new);
+                m_run = m_new;
+            }
+            const float mu = m_run == -INFINITY ? 0.f : m_run;
+            float sum = 0.f;
+            uint32_t pk[BN / 2];
+#pragma unroll
+            for (int c = 0; c < BN; c += 2) {
+                const float p0 = exp2_approx(fmaf(s[c], sl2, -mu));
+                const float p1 = exp2_approx(fmaf(s[c + 1], sl2, -mu));
+                sum += p0 + p1;
+                pk[c >> 1] = pack_bf16(p0, p1);
+            }
+            l_run = l_run * alpha + sum;
+            if (j > 0) { // PV_{j-1} must be done: P buffer free, O settled
+                if (!mbar_wait(&bar->o_done, (j - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int c = 0; c < HD / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(trow + COL_O + c * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(trow + COL_O + c * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            // P row -> shared memory, K-major with 128-byte swizzle
+#pragma unroll
+            for (int ch = 0; ch < BN / 8; ++ch) {
+                uint8_t *dst = prow0 + (ch >> 3) * BOX_BYTES + ((((ch & 7) ^ r) & 7) << 4);
+                *reinterpret_cast<uint4 *>(dst) =
+                    make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->p_full);
+        }
+        if (ok && mbar_wait(&bar->o_done, (n_tiles - 1) & 1)) {
+            tc_fence_after();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            uint4 *orow = reinterpret_cast<uint4 *>(out + ((size_t)(q0 + i) * a.num_heads + h) * HD);
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(trow + COL_O + c * 32, o);
+                tmem_ld_wait();
+                if (r < rows_here) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8)
+                        orow[(c * 32 + e) / 8] = make_uint4(
+                            pack_bf16(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
+                            pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                            pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                            pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+                }
+            }
+        } else {
+            ok = false;
+        }
+    }
+    if (!ok && lane == 0) flag_error(a.dev_err, PA_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace
+
+int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                       const CUtensorMap &tm_v, cudaStream_t s)
+{
+    if (a.head_dim != HD) return PA_ERR_UNSUPPORTED;
+    if (a.max_q <= 0) return PA_OK;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(varlen_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess)
+            return PA_ERR_LAUNCH;
+        attr_set = true;
+    }
+    const unsigned tiles = (unsigned)((a.max_q + BM - 1) / BM);
+    if (tiles > 65535u || a.batch > 65535) return PA_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)a.num_heads, tiles, (unsigned)a.batch);
+    varlen_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tm_q, tm_k, tm_v, a);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }
 
 }  // namespace pa
