@@ -126,6 +126,36 @@ int pa_decode(const void *q, void *k_cache, void *v_cache, const int32_t *block_
               void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
 
 /*
+ * pa_decode without a workspace argument, for callers that cannot allocate
+ * device memory when they call: a runtime with its own fixed memory budget
+ * and no allocator at hand, a plugin handed only its input and output
+ * buffers, or code on a path where cudaMalloc is not allowed or would
+ * stall the device.  The pages have no counterpart to this entry point; it
+ * is a deployment convenience.
+ *
+ * Same arguments and results as pa_decode with dtype PA_BF16 (bf16 only).
+ * The split-K scratch is a 16 MiB array inside the library (device memory
+ * reserved on every GPU that loads the library, held until the process
+ * exits); the caller still passes every input and output.  Sizes whose
+ * scratch need (pa_decode_workspace_size) exceeds 16 MiB are rejected with
+ * PA_ERR_WORKSPACE before anything is launched.  The call allocates nothing
+ * (no cudaMalloc/cudaFree, no allocating library routine); it clears the
+ * merge counters it uses with cudaMemsetAsync on `stream`.
+ *
+ * The first call on each device looks up the array's device address with
+ * that device current (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  All calls share the one array per device, which keeps
+ * the previous call's contents: calls that may overlap on the GPU (different
+ * streams without ordering) race on it and must be serialised by the caller.
+ */
+int pa_decode_static_scratch(const void *q, void *k_cache, void *v_cache,
+                             const int32_t *block_table, const int32_t *cache_seqlens,
+                             const void *k_new, const void *v_new, void *out, int batch,
+                             int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                             int block_size, int max_blocks_per_seq, float softmax_scale,
+                             int32_t *dev_err, void *stream);
+
+/*
  * Varlen cache update ("Jalur Varlen" -> "Perilaku cache").
  *
  * k_chunk, v_chunk [total_q, num_kv_heads, head_dim]: the new tokens of all

@@ -21,7 +21,8 @@ import threading
 import torch
 
 __all__ = [
-    "PAError", "library_path", "load", "pa_decode", "pa_cache_update", "pa_varlen",
+    "PAError", "library_path", "load", "pa_decode", "pa_decode_static_scratch",
+    "pa_cache_update", "pa_varlen",
     "pa_decode_workspace_size", "pa_status_string", "pa_version", "DEVERR_BAD_BLOCK",
     "DEVERR_OVERFLOW", "DEVERR_BAD_CU", "DEVERR_TIMEOUT",
 ]
@@ -63,6 +64,8 @@ def load():
         lib.pa_decode_workspace_size.restype = sz
         lib.pa_decode.argtypes = [p] * 8 + [i] * 7 + [i, f, p, sz, p, p]
         lib.pa_decode.restype = i
+        lib.pa_decode_static_scratch.argtypes = [p] * 8 + [i] * 7 + [f, p, p]
+        lib.pa_decode_static_scratch.restype = i
         lib.pa_cache_update.argtypes = [p] * 10 + [i] * 8 + [i, p, p]
         lib.pa_cache_update.restype = i
         lib.pa_varlen.argtypes = [p] * 5 + [i] * 3 + [p] + [i] * 6 + [i, f, p, p]
@@ -179,6 +182,29 @@ def pa_decode(q, k_cache, v_cache, block_table, cache_seqlens, k_new, v_new, out
                        nb, bs, mb, dt, float(softmax_scale), _ptr(workspace), wbytes,
                        _ptr(dev_err), _stream(stream))
     _call("pa_decode", rc)
+    return out
+
+
+def pa_decode_static_scratch(q, k_cache, v_cache, block_table, cache_seqlens, k_new, v_new,
+                             out=None, softmax_scale: float = 0.0, dev_err=None, stream=None):
+    """pa_decode (bf16) with the library's built-in 16 MiB scratch instead
+    of a workspace: for callers that cannot allocate device memory at call
+    time.  Calls that may overlap on the GPU must be serialised."""
+    _check_dev(q, k_cache, v_cache, block_table, cache_seqlens, k_new, v_new, out, dev_err)
+    _i32(block_table, "block_table")
+    _i32(cache_seqlens, "cache_seqlens")
+    _i32(dev_err, "dev_err")
+    if q.dtype != torch.bfloat16:
+        raise TypeError("pa_decode_static_scratch takes bfloat16 tensors")
+    b, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    rc = load().pa_decode_static_scratch(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                         _ptr(cache_seqlens), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                         b, hq, hkv, d, nb, bs, block_table.shape[1],
+                                         float(softmax_scale), _ptr(dev_err), _stream(stream))
+    _call("pa_decode_static_scratch", rc)
     return out
 
 
