@@ -234,12 +234,15 @@ int pa_varlen(const void *q, const void *k, const void *v, const int32_t *cu_seq
     if (head_dim != 128) return PA_ERR_UNSUPPORTED;
     CUtensorMap tm_q, tm_k, tm_v;
     int rc;
-    if ((rc = encode_rows_map(&tm_q, q, (uint64_t)total_q, num_heads, head_dim, 128)) != PA_OK)
+    if ((rc = encode_rows_map(&tm_q, q, (uint64_t)total_q, num_heads, head_dim, kVarlenQRows)) !=
+        PA_OK)
         return rc;
     if (total_k > 0) {
-        if ((rc = encode_rows_map(&tm_k, k, (uint64_t)total_k, num_kv_heads, head_dim, 128)) != PA_OK)
+        if ((rc = encode_rows_map(&tm_k, k, (uint64_t)total_k, num_kv_heads, head_dim,
+                                 kVarlenKRows)) != PA_OK)
             return rc;
-        if ((rc = encode_rows_map(&tm_v, v, (uint64_t)total_k, num_kv_heads, head_dim, 128)) != PA_OK)
+        if ((rc = encode_rows_map(&tm_v, v, (uint64_t)total_k, num_kv_heads, head_dim,
+                                 kVarlenKRows)) != PA_OK)
             return rc;
     } else {
         tm_k = tm_q;

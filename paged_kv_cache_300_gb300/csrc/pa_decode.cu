@@ -606,17 +606,27 @@ template <int D, int BS, int HS>
 int launch_bf16(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &tm_k,
                 const CUtensorMap &tm_v, cudaStream_t s)
 {
-    auto kern = decode_bf16_kernel<D, BS, HS>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)plan.smem_bytes) != cudaSuccess)
-        return PA_ERR_LAUNCH;
-    kern<<<plan.ctas, Geom<D, BS, HS>::THREADS, plan.smem_bytes, s>>>(tm_k, tm_v, a);
+    // the shared-memory attribute was set when the plan was made
+    decode_bf16_kernel<D, BS, HS><<<plan.ctas, Geom<D, BS, HS>::THREADS, plan.smem_bytes, s>>>(
+        tm_k, tm_v, a);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }
+
+// Resident CTAs per SM of one instantiation on the current device.  The
+// first query per (device, instantiation) also raises the kernel's dynamic
+// shared-memory limit; later calls read the cached answer, so the per-call
+// host cost of a decode launch is a few table lookups.
+constexpr int kMaxDev = 64;
+int g_occ_cache[kMaxDev][2][2][4];
 
 template <int D, int BS, int HS>
 int occupancy_of(size_t smem)
 {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    int &slot = g_occ_cache[dev][D == 128][BS == 32][HS == 8 ? 3 : HS == 4 ? 2 : HS == 2 ? 1 : 0];
+    const int cached = __atomic_load_n(&slot, __ATOMIC_ACQUIRE);
+    if (cached > 0) return cached;
     auto kern = decode_bf16_kernel<D, BS, HS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -625,6 +635,7 @@ int occupancy_of(size_t smem)
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Geom<D, BS, HS>::THREADS, smem) !=
         cudaSuccess)
         return 0;
+    __atomic_store_n(&slot, n, __ATOMIC_RELEASE);
     return n;
 }
 

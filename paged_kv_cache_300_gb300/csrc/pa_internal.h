@@ -86,6 +86,10 @@ struct VarlenArgs {
     int batch, total_q, total_k, num_heads, num_kv_heads, head_dim, max_q, max_k, causal;
     float scale, scale_log2;
 };
+// Rows of one TMA box of the tensor-core varlen kernel: query tiles are 128
+// rows, key/value tiles 64 rows.
+constexpr int kVarlenQRows = 128;
+constexpr int kVarlenKRows = 64;
 int varlen_f32_launch(const VarlenArgs &a, cudaStream_t s);
 int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                        const CUtensorMap &tm_v, cudaStream_t s);

@@ -10,26 +10,31 @@
 // side by side and share them through L2.  Query tiles are issued from the
 // last (most keys under the causal mask) to the first.
 //
-// Warp roles (192 threads):
+// Warp roles (192 threads; two CTAs share an SM, 96 KB of shared memory and
+// 256 TMEM columns each, so one CTA's softmax overlaps the other's MMAs):
 //   warps 0-3  softmax: thread r owns query row r of the tile, which is TMEM
-//              lane r.  It reads its row of S from TMEM, masks, keeps the
-//              running max/sum in registers (exp2 domain), writes P (bf16)
-//              into shared memory in the 128-byte-swizzled K-major layout the
-//              tensor core reads, rescales its row of O in TMEM when the
-//              running max grew by more than 2^8 (lazy rescale: P is then
-//              computed against a max up to 8 below the true one, which the
-//              final division by the same running sum cancels exactly), and
-//              in the end divides O by the sum and stores the row.
-//   warp 4     TMA producer: the Q tile once, then K and V tiles of 128 keys
-//              (two 64-dim swizzled boxes each) into a 2-stage ring.
+//              lane r.  It reads its row of S_j from TMEM, masks, keeps the
+//              running max/sum in registers (exp2 domain), writes P_j as bf16
+//              pairs back over the first half of its S_j row (the tensor core
+//              reads it from there as the A operand), rescales its row of O in
+//              TMEM when the running max grew by more than 2^8 (lazy rescale:
+//              P is then computed against a max up to 8 below the true one,
+//              which the final division by the same running sum cancels
+//              exactly), and in the end divides O by the sum and stores the row.
+//   warp 4     TMA producer: the Q tile (128 rows) once, then K and V tiles of
+//              64 keys (two 64-dim swizzled boxes each) into separate 2-stage
+//              rings.  A K stage frees as soon as S_j = Q K_j^T is computed, a
+//              V stage when O += P_j V_j is, so the next K load overlaps the
+//              softmax instead of waiting for PV.
 //   warp 5     TMEM allocator and MMA issuer (one thread): S_j = Q K_j^T into
-//              one of two TMEM S buffers (M=128, N=128, K=16 per instruction,
-//              both operands K-major), then O += P_j V_j with V read MN-major
-//              straight from its TMA tile; tcgen05.commit signals mbarriers.
-// S_{j+1} is computed while the softmax warps work on S_j.
+//              one of two TMEM S buffers (M=128, N=64, K=16 per instruction,
+//              both operands K-major from shared memory), then O += P_j V_j
+//              (M=128, N=128) with P_j from TMEM and V read MN-major straight
+//              from its TMA tile; tcgen05.commit signals the mbarriers.  S_{j+1}
+//              is computed while the softmax warps work on S_j.
 //
-// TMEM: columns [0,128) and [128,256) hold the two S buffers, [256,384) O.
-// Every mbarrier wait is bounded; on timeout the kernel flags
+// TMEM: columns [0,64) and [64,128) hold the two S (then P) buffers,
+// [128,256) O.  Every mbarrier wait is bounded; on timeout the kernel flags
 // PA_DEVERR_TIMEOUT, frees its TMEM and returns.
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -39,48 +44,51 @@
 namespace pa {
 namespace {
 
-constexpr int BM = 128;                  // query rows per tile (TMEM lanes)
-constexpr int BN = 128;                  // keys per tile
-constexpr int HD = 128;                  // head_dim
-constexpr int BOX_BYTES = 128 * 128;     // 128 rows x 64 dims bf16, 128-byte swizzled
-constexpr int TILE_BYTES = 2 * BOX_BYTES; // 128 rows x 128 dims
+constexpr int BM = kVarlenQRows;              // query rows per tile (TMEM lanes)
+constexpr int BN = kVarlenKRows;              // keys per tile
+constexpr int HD = 128;                       // head_dim
+constexpr int QBOX = BM * 128;                // 128 rows x 64 dims bf16, 128-byte swizzled
+constexpr int KBOX = BN * 128;                // 64 keys x 64 dims
+constexpr int Q_BYTES = 2 * QBOX;             // the query tile: two 64-dim boxes
+constexpr int KV_BYTES = 2 * KBOX;            // one K (or V) tile of 64 keys
 constexpr int NSTAGE = 2;
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE_BYTES;
-constexpr int OFF_V = OFF_K + NSTAGE * TILE_BYTES;
-constexpr int OFF_P = OFF_V + NSTAGE * TILE_BYTES;
-constexpr int OFF_BAR = OFF_P + TILE_BYTES;
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024; // + alignment slack
+constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_V = OFF_K + NSTAGE * KV_BYTES;
+constexpr int OFF_BAR = OFF_V + NSTAGE * KV_BYTES;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024; // + alignment slack: two CTAs per SM
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_O = 256;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t COL_O = 2 * BN;
 constexpr float kRescaleThreshold = 8.0f; // log2 units
 
 struct Barriers {
     uint64_t q_full;
     uint64_t k_full[NSTAGE];
     uint64_t v_full[NSTAGE];
-    uint64_t kv_empty[NSTAGE];
+    uint64_t k_empty[NSTAGE];
+    uint64_t v_empty[NSTAGE];
     uint64_t s_full[2];
     uint64_t p_full;
     uint64_t o_done;
     uint32_t tmem_base;
 };
 
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk)
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk, uint32_t box_bytes)
 {
-    // kk-th 16-element slice of K inside a [128 rows][128] K-major tile made
-    // of two 64-element boxes: box kk / 4, 32 bytes per slice inside a row.
-    return umma_desc_sw128(tile + (uint32_t)(kk >> 2) * BOX_BYTES + (uint32_t)(kk & 3) * 32u, 16u,
+    // kk-th 16-element slice of the reduction dimension inside a K-major tile
+    // made of 64-element boxes of `box_bytes`: box kk / 4, 32 bytes per slice
+    // inside a 128-byte row; 8-row groups are 1024 bytes apart.
+    return umma_desc_sw128(tile + (uint32_t)(kk >> 2) * box_bytes + (uint32_t)(kk & 3) * 32u, 16u,
                            1024u);
 }
 
 __device__ __forceinline__ uint64_t v_desc(uint32_t tile, int kk)
 {
-    // V tile [128 keys][128 dims] read as the MN-major B operand (N = dims):
+    // V tile [64 keys][128 dims] read as the MN-major B operand (N = dims):
     // 16 keys per instruction = two 8-row groups (SBO 1024 B); the second
-    // 64-dim box is LBO = 16 KB away.
-    return umma_desc_sw128(tile + (uint32_t)kk * 2048u, (uint32_t)BOX_BYTES, 1024u);
+    // 64-dim box is LBO = KBOX bytes away.
+    return umma_desc_sw128(tile + (uint32_t)kk * 2048u, (uint32_t)KBOX, 1024u);
 }
 
 }  // namespace
@@ -89,7 +97,7 @@ __device__ __forceinline__ uint64_t v_desc(uint32_t tile, int kk)
 namespace pa {
 namespace {
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     varlen_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const VarlenArgs a)
 {
@@ -133,7 +141,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&bar->k_full[s], 1);
             mbar_init(&bar->v_full[s], 1);
-            mbar_init(&bar->kv_empty[s], 1);
+            mbar_init(&bar->k_empty[s], 1);
+            mbar_init(&bar->v_empty[s], 1);
         }
         mbar_init(&bar->s_full[0], 1);
         mbar_init(&bar->s_full[1], 1);
@@ -154,24 +163,30 @@ __global__ void __launch_bounds__(THREADS, 1)
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(&bar->q_full, TILE_BYTES);
+            mbar_arrive_expect_tx(&bar->q_full, Q_BYTES);
             for (int c = 0; c < 2; ++c)
-                tma_load_3d(sbase + OFF_Q + c * BOX_BYTES, &tm_q, &bar->q_full, 0, h * 2 + c,
+                tma_load_3d(sbase + OFF_Q + c * QBOX, &tm_q, &bar->q_full, 0, h * 2 + c,
                             q0 + m * BM);
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const int st = j & 1;
-                if (j >= NSTAGE && !mbar_wait(&bar->kv_empty[st], ((j >> 1) - 1) & 1)) {
+                // K_j's stage frees when S_{j-2} is computed, V_j's when
+                // PV_{j-2} is done
+                if (j >= NSTAGE && !mbar_wait(&bar->k_empty[st], ((j >> 1) - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 const int row = k0 + j * BN;
-                mbar_arrive_expect_tx(&bar->k_full[st], TILE_BYTES);
+                mbar_arrive_expect_tx(&bar->k_full[st], KV_BYTES);
                 for (int c = 0; c < 2; ++c)
-                    tma_load_3d(sbase + OFF_K + st * TILE_BYTES + c * BOX_BYTES, &tm_k,
+                    tma_load_3d(sbase + OFF_K + st * KV_BYTES + c * KBOX, &tm_k,
                                 &bar->k_full[st], 0, kvh * 2 + c, row);
-                mbar_arrive_expect_tx(&bar->v_full[st], TILE_BYTES);
+                if (j >= NSTAGE && !mbar_wait(&bar->v_empty[st], ((j >> 1) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bar->v_full[st], KV_BYTES);
                 for (int c = 0; c < 2; ++c)
-                    tma_load_3d(sbase + OFF_V + st * TILE_BYTES + c * BOX_BYTES, &tm_v,
+                    tma_load_3d(sbase + OFF_V + st * KV_BYTES + c * KBOX, &tm_v,
                                 &bar->v_full[st], 0, kvh * 2 + c, row);
             }
         }
@@ -181,18 +196,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, 0, 0);
             constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, HD, 0, 1);
-            const uint32_t qs = sbase + OFF_Q, ps = sbase + OFF_P;
+            const uint32_t qs = sbase + OFF_Q;
             ok = mbar_wait(&bar->q_full, 0);
             auto issue_qk = [&](int j) -> bool {
                 const int st = j & 1;
                 if (!mbar_wait(&bar->k_full[st], (j >> 1) & 1)) return false;
                 tc_fence_after();
-                const uint32_t ks = sbase + OFF_K + st * TILE_BYTES;
+                const uint32_t ks = sbase + OFF_K + st * KV_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
-                    umma_bf16(tmem + st * BN, kmajor_desc(qs, kk), kmajor_desc(ks, kk), idesc_qk,
-                              kk > 0);
+                    umma_bf16(tmem + st * BN, kmajor_desc(qs, kk, QBOX), kmajor_desc(ks, kk, KBOX),
+                              idesc_qk, kk > 0);
                 umma_commit(&bar->s_full[st]);
+                umma_commit(&bar->k_empty[st]);
                 return true;
             };
             if (ok) ok = issue_qk(0);
@@ -204,18 +220,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t vs = sbase + OFF_V + st * TILE_BYTES;
+                // P_j (bf16, 32 columns) overwrote the first half of S_j in TMEM
+                const uint32_t pt = tmem + st * BN;
+                const uint32_t vs = sbase + OFF_V + st * KV_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_bf16(tmem + COL_O, kmajor_desc(ps, kk), v_desc(vs, kk), idesc_pv,
-                              (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_tmem_a(tmem + COL_O, pt + kk * 8, v_desc(vs, kk), idesc_pv,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&bar->o_done);
-                umma_commit(&bar->kv_empty[st]);
+                umma_commit(&bar->v_empty[st]);
             }
             // the producer never waits for the last two stage releases: wait
             // here so that no commit arrives after the CTA has left
             for (int t = max(0, n_tiles - 2); t < n_tiles && ok; ++t)
-                ok = mbar_wait(&bar->kv_empty[t & 1], (t >> 1) & 1);
+                ok = mbar_wait(&bar->k_empty[t & 1], (t >> 1) & 1) &&
+                     mbar_wait(&bar->v_empty[t & 1], (t >> 1) & 1);
         }
         __syncwarp();
     } else {
@@ -226,7 +245,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         const float sl2 = a.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
-        uint8_t *prow0 = smem + OFF_P + r * 128;
         for (int j = 0; j < n_tiles; ++j) {
             const int st = j & 1;
             if (!mbar_wait(&bar->s_full[st], (j >> 1) & 1)) {
@@ -269,7 +287,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 pk[c >> 1] = pack_bf16(p0, p1);
             }
             l_run = l_run * alpha + sum;
-            if (j > 0) { // PV_{j-1} must be done: P buffer free, O settled
+            // P row (bf16 pairs) over the S_j row it came from; PV_j reads it
+            // as the TMEM A operand.  Its own buffer: no wait on PV_{j-1}.
+            tmem_st32(trow + st * BN, pk);
+            if (j > 0) { // PV_{j-1} must be done before O is rescaled and P_j released
                 if (!mbar_wait(&bar->o_done, (j - 1) & 1)) {
                     ok = false;
                     break;
@@ -286,17 +307,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                             o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                         tmem_st32(trow + COL_O + c * 32, o);
                     }
-                    tmem_st_wait();
                 }
             }
-            // P row -> shared memory, K-major with 128-byte swizzle
-#pragma unroll
-            for (int ch = 0; ch < BN / 8; ++ch) {
-                uint8_t *dst = prow0 + (ch >> 3) * BOX_BYTES + ((((ch & 7) ^ r) & 7) << 4);
-                *reinterpret_cast<uint4 *>(dst) =
-                    make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-            }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar->p_full);
