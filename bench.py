@@ -133,7 +133,7 @@ class L2Flush:
 
     def zero_(self):
         self.w.zero_()
-        self.torch.sum(self.r, out=self.acc)
+        self.torch.sum(self.r, dim=(0,), out=self.acc)
 
 
 # --------------------------------------------------------------------------
