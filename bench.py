@@ -148,31 +148,37 @@ class Dist:
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
 
-    def init(self, torch):
+    def init(self, torch, backend: str = "nccl"):
+        """nccl on GPUs; gloo (CPU tensors) for the host-side tests."""
+        self.device = "cuda" if backend == "nccl" else "cpu"
         if self.world > 1:
             import torch.distributed as dist
             os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-            torch.cuda.set_device(self.local)
-            dist.init_process_group("nccl", rank=self.rank, world_size=self.world)
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend, rank=self.rank, world_size=self.world)
             self.pg = dist
 
     def barrier(self, torch):
         if self.pg is not None:
             self.pg.barrier()
 
-    def max(self, torch, x: float) -> float:
+    def _reduce(self, torch, x: float, op) -> float:
         if self.pg is None:
             return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self.pg.all_reduce(t, op=op)
         return float(t.item())
 
+    def max(self, torch, x: float) -> float:
+        return self._reduce(torch, x, None if self.pg is None else self.pg.ReduceOp.MAX)
+
     def sum(self, torch, x: float) -> float:
-        if self.pg is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
-        return float(t.item())
+        return self._reduce(torch, x, None if self.pg is None else self.pg.ReduceOp.SUM)
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
 
 
 # --------------------------------------------------------------------------
@@ -438,8 +444,8 @@ def main(argv=None):
                               "tflops": round(flops / att_ms / 1e9, 2), "clocks": clk}))
         return 0
 
-    # ---- main line: decode workload 2
-    case = decode_config(2)
+    # ---- main line: decode workload 2 (each rank decodes its own batch)
+    case = decode_config(2, seed_offset=dist.rank)
     res = run_decode_leg(torch, pa, case, args.steps, args.warmup, flush, dist, sync_ranks=True)
     dev_ms_total = dist.max(torch, sum(res["ms"]))
     ms = dev_ms_total / args.steps

@@ -276,11 +276,13 @@ WORKED_EXAMPLE_TABLE = [[2, -1, -1, -1], [0, 1, -1, -1], [3, 5, 6, -1]]
 WORKED_EXAMPLE_SEQLENS = [30, 32, 70]
 
 
-def decode_config(idx: int, scale_down: int = 1) -> DecodeCase:
+def decode_config(idx: int, scale_down: int = 1, seed_offset: int = 0) -> DecodeCase:
     """Decode workloads 1, 2, 3 and 5.  `scale_down` > 1 keeps the structure
     (heads, head_dim, block size, length distribution) with fewer sequences,
-    for oracle runs that must finish in seconds."""
-    seed = 1000 + idx
+    for oracle runs that must finish in seconds.  `seed_offset` draws another
+    batch of the same workload (one per rank when the benchmark runs on
+    several GPUs)."""
+    seed = 1000 + idx + 100 * seed_offset
     if idx == 1:
         return make_decode(seed, WORKED_EXAMPLE_SEQLENS, 4, 2, 64, 32, dtype=torch.float32,
                            block_table=WORKED_EXAMPLE_TABLE, num_blocks=8, name=CONFIG_NAMES[1])
