@@ -51,7 +51,10 @@ def source_hash(name: str) -> str:
 
 # DRAM traffic per launch taken from ncu captures (profiles/), valid only for
 # the kernel source they were measured on.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("pa_decode.cu", "workload2"): {"src": "2036b8eb8d4720af", "bytes": 560_344_832},
+    ("pa_varlen_tc.cu", "workload4"): {"src": "85ddcda18cc81525", "bytes": 661_891_072},
+}
 
 
 def traffic_for(kernel_file: str, workload: str):
@@ -481,7 +484,9 @@ def main(argv=None):
                 "tflops": round(flops / att_ms / 1e9, 2),
                 "roofline": {"bound": "tensor", "achieved": round(flops / att_ms / 1e9, 2),
                              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                             "frac": round(flops / att_ms / 1e9 / peaks["bf16_tflops"], 4)},
+                             "frac": round(flops / att_ms / 1e9 / peaks["bf16_tflops"], 4),
+                             "traffic": traffic_for("pa_varlen_tc.cu", "workload4"),
+                             "peak_source": f"{peak_kind} bf16_tflops (burst)"},
                 "cache_update_GBps": round(upd_bytes / upd_ms / 1e6, 1),
                 "step_tflops": round(flops / (att_ms + upd_ms) / 1e9, 2),
             }
