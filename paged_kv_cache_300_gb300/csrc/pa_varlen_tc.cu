@@ -21,17 +21,18 @@
 //              P is then computed against a max up to 8 below the true one,
 //              which the final division by the same running sum cancels
 //              exactly), and in the end divides O by the sum and stores the row.
-//   warp 4     TMA producer: the Q tile (128 rows) once, then K and V tiles of
-//              64 keys (two 64-dim swizzled boxes each) into separate 2-stage
-//              rings.  A K stage frees as soon as S_j = Q K_j^T is computed, a
-//              V stage when O += P_j V_j is, so the next K load overlaps the
-//              softmax instead of waiting for PV.
+//   warp 4     TMA producers: lane 0 loads the Q tile (128 rows) once, then
+//              K tiles of 64 keys (two 64-dim swizzled boxes each); lane 1
+//              loads the V tiles.  Separate 2-stage rings: a K stage frees as
+//              soon as S_j = Q K_j^T is computed, a V stage when O += P_j V_j
+//              is, so K loads run a whole tile ahead.
 //   warp 5     TMEM allocator and MMA issuer (one thread): S_j = Q K_j^T into
 //              one of two TMEM S buffers (M=128, N=64, K=16 per instruction,
 //              both operands K-major from shared memory), then O += P_j V_j
 //              (M=128, N=128) with P_j from TMEM and V read MN-major straight
-//              from its TMA tile; tcgen05.commit signals the mbarriers.  S_{j+1}
-//              is computed while the softmax warps work on S_j.
+//              from its TMA tile; tcgen05.commit signals the mbarriers.  S_0
+//              and S_1 are issued first, then S_{j+2} right after PV_j, so
+//              S_{j+1} is ready while the softmax warps work on S_j.
 //
 // TMEM: columns [0,64) and [64,128) hold the two S (then P) buffers,
 // [128,256) O.  Every mbarrier wait is bounded; on timeout the kernel flags
@@ -158,28 +159,33 @@ __global__ void __launch_bounds__(THREADS, 2)
     bool ok = true;
 
     if (warp == 4) {
-        // ================= TMA producer =================
+        // ================= TMA producers =================
+        // lane 0 streams Q and the K ring, lane 1 the V ring, so that a K
+        // load never waits behind a V stage that frees later
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
             mbar_arrive_expect_tx(&bar->q_full, Q_BYTES);
             for (int c = 0; c < 2; ++c)
                 tma_load_3d(sbase + OFF_Q + c * QBOX, &tm_q, &bar->q_full, 0, h * 2 + c,
                             q0 + m * BM);
-            for (int j = 0; j < n_tiles && ok; ++j) {
+            for (int j = 0; j < n_tiles; ++j) {
                 const int st = j & 1;
-                // K_j's stage frees when S_{j-2} is computed, V_j's when
-                // PV_{j-2} is done
+                // K_j's stage frees when S_{j-2} has been computed
                 if (j >= NSTAGE && !mbar_wait(&bar->k_empty[st], ((j >> 1) - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                const int row = k0 + j * BN;
                 mbar_arrive_expect_tx(&bar->k_full[st], KV_BYTES);
                 for (int c = 0; c < 2; ++c)
                     tma_load_3d(sbase + OFF_K + st * KV_BYTES + c * KBOX, &tm_k,
-                                &bar->k_full[st], 0, kvh * 2 + c, row);
+                                &bar->k_full[st], 0, kvh * 2 + c, k0 + j * BN);
+            }
+        } else if (lane == 1) {
+            prefetch_tmap(&tm_v);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j & 1;
+                // V_j's stage frees when PV_{j-2} is done
                 if (j >= NSTAGE && !mbar_wait(&bar->v_empty[st], ((j >> 1) - 1) & 1)) {
                     ok = false;
                     break;
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                 mbar_arrive_expect_tx(&bar->v_full[st], KV_BYTES);
                 for (int c = 0; c < 2; ++c)
                     tma_load_3d(sbase + OFF_V + st * KV_BYTES + c * KBOX, &tm_v,
-                                &bar->v_full[st], 0, kvh * 2 + c, row);
+                                &bar->v_full[st], 0, kvh * 2 + c, k0 + j * BN);
             }
         }
         __syncwarp();
@@ -211,10 +217,14 @@ __global__ void __launch_bounds__(THREADS, 2)
                 umma_commit(&bar->k_empty[st]);
                 return true;
             };
+            // S_0 and S_1 up front; afterwards S_{j+2} is issued right after
+            // PV_j (which consumes P_j from the same TMEM columns; the tensor
+            // pipe executes one thread's MMAs in order), so every K load has
+            // a whole tile of slack and PV_j never waits behind a K load
             if (ok) ok = issue_qk(0);
+            if (ok && n_tiles > 1) ok = issue_qk(1);
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const int st = j & 1;
-                if (j + 1 < n_tiles && !(ok = issue_qk(j + 1))) break;
                 if (!mbar_wait(&bar->p_full, j & 1) || !mbar_wait(&bar->v_full[st], (j >> 1) & 1)) {
                     ok = false;
                     break;
@@ -229,6 +239,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                                      (j > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&bar->o_done);
                 umma_commit(&bar->v_empty[st]);
+                if (j + 2 < n_tiles && !(ok = issue_qk(j + 2))) break;
             }
             // the producer never waits for the last two stage releases: wait
             // here so that no commit arrives after the CTA has left
@@ -258,17 +269,21 @@ __global__ void __launch_bounds__(THREADS, 2)
                 tmem_ld32(trow + st * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
             tmem_ld_wait();
             const int kb = j * BN;
-            float mx = -INFINITY;
-            if (kb + BN - 1 <= lim) {
+            if (kb + BN - 1 > lim) {
 #pragma unroll
-                for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
+                for (int c = 0; c < BN; ++c)
                     if (kb + c > lim) s[c] = -INFINITY;
-                    mx = fmaxf(mx, s[c]);
-                }
             }
+            // row max as 8 independent chains (short critical path)
+            float mx8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx8[u] = s[u];
+#pragma unroll
+            for (int c = 8; c < BN; c += 8)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], s[c + u]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_new = fmaxf(m_run, mx * sl2);
             const bool need = m_new > m_run + kRescaleThreshold;
             float alpha = 1.f;
@@ -277,15 +292,16 @@ __global__ void __launch_bounds__(THREADS, 2)
                 m_run = m_new;
             }
             const float mu = m_run == -INFINITY ? 0.f : m_run;
-            float sum = 0.f;
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f}; // 4 independent partial sums
             uint32_t pk[BN / 2];
 #pragma unroll
             for (int c = 0; c < BN; c += 2) {
                 const float p0 = exp2_approx(fmaf(s[c], sl2, -mu));
                 const float p1 = exp2_approx(fmaf(s[c + 1], sl2, -mu));
-                sum += p0 + p1;
+                sum4[(c >> 1) & 3] += p0 + p1;
                 pk[c >> 1] = pack_bf16(p0, p1);
             }
+            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             l_run = l_run * alpha + sum;
             // P row (bf16 pairs) over the S_j row it came from; PV_j reads it
             // as the TMEM A operand.  Its own buffer: no wait on PV_{j-1}.
@@ -337,7 +353,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             ok = false;
         }
     }
-    if (!ok && lane == 0) flag_error(a.dev_err, PA_DEVERR_TIMEOUT);
+    if (!ok) flag_error(a.dev_err, PA_DEVERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
