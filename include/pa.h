@@ -192,6 +192,33 @@ int pa_varlen(const void *q, const void *k, const void *v, const int32_t *cu_seq
               void *out, int batch, int total_q, int total_k, int num_heads, int num_kv_heads,
               int head_dim, pa_dtype dtype, float softmax_scale, int32_t *dev_err, void *stream);
 
+/*
+ * Varlen attention that reads each request's keys straight from the paged
+ * pool through its block_table row, with no packed copy: "Perhatian
+ * berhalaman", section "Jalur Varlen" -> "Perilaku cache" names the manual
+ * cache read of the varlen path as a bottleneck at long lengths, and
+ * "39 · PagedAttention" (inference-notes), section "Ghi chú", notes that
+ * attention kernels can take the block table directly.  Typical use: scatter
+ * the new chunk with pa_cache_update (k_full/v_full NULL), then call this.
+ *
+ * Request r owns q rows [cu_seq_lens_q[r], cu_seq_lens_q[r+1]) of q/out
+ * [total_q, num_heads, head_dim]; its keys are logical positions
+ * 0 .. seqlens_k[r]-1 of block_table row r in k_cache/v_cache
+ * [num_blocks, block_size, num_kv_heads, head_dim].  Masking, scaling, GQA
+ * mapping and empty rows as pa_varlen; for equal inputs the result equals
+ * pa_varlen on the gathered keys bit for bit.  seqlens_k[r] beyond
+ * max_blocks_per_seq * block_size sets PA_DEVERR_OVERFLOW and zeroes the
+ * request's rows; a needed entry that is not a valid block sets
+ * PA_DEVERR_BAD_BLOCK and zeroes the affected query tiles.
+ * Supported: PA_BF16, head_dim 128, block_size 8, 16, 32 or 64.
+ */
+int pa_varlen_paged(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_table, const int32_t *cu_seq_lens_q,
+                    const int32_t *seqlens_k, int max_length_q, int max_length_k, int causal,
+                    void *out, int batch, int total_q, int num_heads, int num_kv_heads,
+                    int head_dim, int num_blocks, int block_size, int max_blocks_per_seq,
+                    pa_dtype dtype, float softmax_scale, int32_t *dev_err, void *stream);
+
 /* Static description of a status code (never NULL). */
 const char *pa_status_string(int status);
 

@@ -11,6 +11,7 @@ built, or no GPU is present, calls raise.
     pa_cache_update  scatter a packed varlen chunk into the paged pool
                      (optionally gather prefix + chunk into packed k/v)
     pa_varlen        packed variable-length attention (bf16: tcgen05)
+    pa_varlen_paged  the same, reading keys through block_table from the pool
 """
 from __future__ import annotations
 
@@ -22,7 +23,7 @@ import torch
 
 __all__ = [
     "PAError", "library_path", "load", "pa_decode", "pa_decode_static_scratch",
-    "pa_cache_update", "pa_varlen",
+    "pa_cache_update", "pa_varlen", "pa_varlen_paged",
     "pa_decode_workspace_size", "pa_status_string", "pa_version", "DEVERR_BAD_BLOCK",
     "DEVERR_OVERFLOW", "DEVERR_BAD_CU", "DEVERR_TIMEOUT",
 ]
@@ -70,6 +71,8 @@ def load():
         lib.pa_cache_update.restype = i
         lib.pa_varlen.argtypes = [p] * 5 + [i] * 3 + [p] + [i] * 6 + [i, f, p, p]
         lib.pa_varlen.restype = i
+        lib.pa_varlen_paged.argtypes = [p] * 6 + [i] * 3 + [p] + [i] * 8 + [i, f, p, p]
+        lib.pa_varlen_paged.restype = i
         lib.pa_status_string.argtypes = [i]
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_version.argtypes = []
@@ -250,4 +253,29 @@ def pa_varlen(q, k, v, cu_seq_lens_q, cu_seq_lens_k, max_length_q: int, max_leng
                           cu_seq_lens_q.shape[0] - 1, tq, tk, hq, hkv, d, dt,
                           float(softmax_scale), _ptr(dev_err), _stream(stream))
     _call("pa_varlen", rc)
+    return out
+
+
+def pa_varlen_paged(q, k_cache, v_cache, block_table, cu_seq_lens_q, seqlens_k,
+                    max_length_q: int, max_length_k: int, causal: bool, out=None,
+                    softmax_scale: float = 0.0, dev_err=None, stream=None):
+    """Varlen attention with keys read through block_table: q [Tq, Hq, D];
+    k_cache/v_cache [NB, bs, Hkv, D]; block_table [B, MB]; seqlens_k [B]
+    (keys of each request in the pool).  Returns out [Tq, Hq, D]."""
+    _check_dev(q, k_cache, v_cache, block_table, cu_seq_lens_q, seqlens_k, out, dev_err)
+    for t, n in ((block_table, "block_table"), (cu_seq_lens_q, "cu_seq_lens_q"),
+                 (seqlens_k, "seqlens_k"), (dev_err, "dev_err")):
+        _i32(t, n)
+    dt = _dtype(q)
+    tq, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    rc = load().pa_varlen_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                _ptr(cu_seq_lens_q), _ptr(seqlens_k), int(max_length_q),
+                                int(max_length_k), int(bool(causal)), _ptr(out),
+                                cu_seq_lens_q.shape[0] - 1, tq, hq, hkv, d, nb, bs,
+                                block_table.shape[1], dt, float(softmax_scale), _ptr(dev_err),
+                                _stream(stream))
+    _call("pa_varlen_paged", rc)
     return out

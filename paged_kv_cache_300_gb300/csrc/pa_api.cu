@@ -251,4 +251,57 @@ int pa_varlen(const void *q, const void *k, const void *v, const int32_t *cu_seq
     return varlen_bf16_launch(a, tm_q, tm_k, tm_v, s);
 }
 
+int pa_varlen_paged(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_table, const int32_t *cu_seq_lens_q,
+                    const int32_t *seqlens_k, int max_length_q, int max_length_k, int causal,
+                    void *out, int batch, int total_q, int num_heads, int num_kv_heads,
+                    int head_dim, int num_blocks, int block_size, int max_blocks_per_seq,
+                    pa_dtype dtype, float softmax_scale, int32_t *dev_err, void *stream)
+{
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (batch < 0 || total_q < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_length_q < 0 || max_length_k < 0 || num_heads % num_kv_heads != 0 ||
+        num_blocks <= 0 || block_size <= 0 || max_blocks_per_seq <= 0)
+        return PA_ERR_SHAPE;
+    if (dtype != PA_BF16 || head_dim != 128 || kVarlenKRows % block_size != 0 || block_size % 8 != 0)
+        return PA_ERR_UNSUPPORTED;
+    if ((long long)num_blocks * block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    if (batch == 0 || total_q == 0) return PA_OK;
+    if (!q || !out || !k_cache || !v_cache || !block_table || !cu_seq_lens_q || !seqlens_k)
+        return PA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_SHAPE;
+    VarlenArgs a{};
+    a.q = q;
+    a.cu_q = cu_seq_lens_q;
+    a.out = out;
+    a.dev_err = dev_err;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.max_q = max_length_q;
+    a.max_k = max_length_k;
+    a.causal = causal != 0;
+    a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
+    a.scale_log2 = a.scale * 1.4426950408889634f;
+    a.block_table = block_table;
+    a.seqlens_k = seqlens_k;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    CUtensorMap tm_q, tm_k, tm_v;
+    int rc;
+    const uint64_t rows = (uint64_t)num_blocks * block_size;
+    if ((rc = encode_rows_map(&tm_q, q, (uint64_t)total_q, num_heads, head_dim, kVarlenQRows)) !=
+        PA_OK)
+        return rc;
+    if ((rc = encode_rows_map(&tm_k, k_cache, rows, num_kv_heads, head_dim, block_size)) != PA_OK)
+        return rc;
+    if ((rc = encode_rows_map(&tm_v, v_cache, rows, num_kv_heads, head_dim, block_size)) != PA_OK)
+        return rc;
+    return varlen_paged_bf16_launch(a, tm_q, tm_k, tm_v, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -85,6 +85,11 @@ struct VarlenArgs {
     int32_t *dev_err;
     int batch, total_q, total_k, num_heads, num_kv_heads, head_dim, max_q, max_k, causal;
     float scale, scale_log2;
+    // paged variant: keys of request r are logical positions 0..seqlens_k[r)-1
+    // of block_table row r in the pool [num_blocks, block_size, Hkv, D]
+    const int32_t *block_table;
+    const int32_t *seqlens_k;
+    int num_blocks, block_size, max_blocks_per_seq;
 };
 // Rows of one TMA box of the tensor-core varlen kernel: query tiles are 128
 // rows, key/value tiles 64 rows.
@@ -93,6 +98,8 @@ constexpr int kVarlenKRows = 64;
 int varlen_f32_launch(const VarlenArgs &a, cudaStream_t s);
 int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                        const CUtensorMap &tm_v, cudaStream_t s);
+int varlen_paged_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q,
+                             const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t s);
 
 // ------------------------------------------------------------------ helpers
 int num_sms();

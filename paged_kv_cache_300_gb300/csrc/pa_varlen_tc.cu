@@ -57,7 +57,9 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + Q_BYTES;
 constexpr int OFF_V = OFF_K + NSTAGE * KV_BYTES;
 constexpr int OFF_BAR = OFF_V + NSTAGE * KV_BYTES;
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024; // + alignment slack: two CTAs per SM
+constexpr int TAB_CAP = 512;                  // block-table entries staged in smem (paged)
+constexpr int OFF_TAB = OFF_BAR + 256;
+constexpr int SMEM_BYTES = OFF_TAB + 4 * TAB_CAP + 1024; // + alignment slack: two CTAs per SM
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t COL_O = 2 * BN;
@@ -73,6 +75,7 @@ struct Barriers {
     uint64_t p_full;
     uint64_t o_done;
     uint32_t tmem_base;
+    int bad_block; // paged variant: a needed table entry was not a valid block
 };
 
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk, uint32_t box_bytes)
@@ -98,6 +101,45 @@ __device__ __forceinline__ uint64_t v_desc(uint32_t tile, int kk)
 namespace pa {
 namespace {
 
+// Loads key/value tile j (64 keys, both 64-dim halves) into `dst`.  Packed:
+// one box per half at row k0 + 64 j.  Paged: the tile's keys are logical
+// positions 64 j .. 64 j + 63 of the request, i.e. 64 / block_size pool
+// blocks resolved through the block table; each block's box lands at its
+// row offset (a multiple of 8 rows, so the 128-byte swizzle phase is the same
+// as for a packed tile).  Positions past the request's keys, and needed
+// entries that are not valid blocks (flagged), read the zero fill of a
+// coordinate past the end of the pool.
+template <bool PAGED>
+__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap *map, uint64_t *full,
+                                             const VarlenArgs &a, int b, int kvh, int k0, int kl,
+                                             int j, int *bad_block, const int *tab)
+{
+    if constexpr (!PAGED) {
+        for (int c = 0; c < 2; ++c)
+            tma_load_3d(dst + c * KBOX, map, full, 0, kvh * 2 + c, k0 + j * BN);
+    } else {
+        const int bs = a.block_size;
+        const int oob = a.num_blocks * bs;
+        for (int i = 0; i < BN / bs; ++i) {
+            const int pos = j * BN + i * bs;
+            int row = oob;
+            if (pos < kl) {
+                const int e = pos / bs;
+                const int p = e < TAB_CAP
+                                  ? tab[e]
+                                  : __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
+                if (p >= 0 && p < a.num_blocks)
+                    row = p * bs;
+                else
+                    *bad_block = 1;
+            }
+            for (int c = 0; c < 2; ++c)
+                tma_load_3d(dst + c * KBOX + i * bs * 128, map, full, 0, kvh * 2 + c, row);
+        }
+    }
+}
+
+template <bool PAGED>
 __global__ void __launch_bounds__(THREADS, 2)
     varlen_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const VarlenArgs a)
@@ -114,13 +156,25 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int G = a.num_heads / a.num_kv_heads, kvh = h / G;
 
     const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
-    const int k0 = __ldg(a.cu_k + b), k1 = __ldg(a.cu_k + b + 1);
-    if (q0 < 0 || q1 < q0 || q1 > a.total_q || k0 < 0 || k1 < k0 || k1 > a.total_k ||
-        q1 - q0 > (int)gridDim.y * BM) {
+    int k0 = 0, kl = 0;
+    bool bad_cu = q0 < 0 || q1 < q0 || q1 > a.total_q || q1 - q0 > (int)gridDim.y * BM;
+    if constexpr (PAGED) {
+        kl = __ldg(a.seqlens_k + b);
+        if (kl < 0 || (long long)kl > (long long)a.max_blocks_per_seq * a.block_size) {
+            if (tid == 0 && h == 0 && m == 0) flag_error(a.dev_err, PA_DEVERR_OVERFLOW);
+            kl = 0; // no keys: the rows below come out as zeros
+        }
+    } else {
+        k0 = __ldg(a.cu_k + b);
+        const int k1 = __ldg(a.cu_k + b + 1);
+        bad_cu |= k0 < 0 || k1 < k0 || k1 > a.total_k;
+        kl = k1 - k0;
+    }
+    if (bad_cu) {
         if (tid == 0 && h == 0 && m == 0) flag_error(a.dev_err, PA_DEVERR_BAD_CU);
         return;
     }
-    const int ql = q1 - q0, kl = k1 - k0;
+    const int ql = q1 - q0;
     if (m * BM >= ql) return;
     const int rows_here = min(BM, ql - m * BM);
     int n_keys = kl;
@@ -149,6 +203,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         mbar_init(&bar->s_full[1], 1);
         mbar_init(&bar->p_full, 4);
         mbar_init(&bar->o_done, 1);
+        bar->bad_block = 0;
         fence_mbar_init();
     }
     if (warp == 5) tmem_alloc(&bar->tmem_base, TMEM_COLS);
@@ -160,6 +215,14 @@ __global__ void __launch_bounds__(THREADS, 2)
 
     if (warp == 4) {
         // ================= TMA producers =================
+        int *tab = reinterpret_cast<int *>(smem + OFF_TAB);
+        if constexpr (PAGED) {
+            // stage this CTA's slice of the block table (coalesced, once)
+            const int need = min(TAB_CAP, (min(kl, n_tiles * BN) + a.block_size - 1) / a.block_size);
+            for (int e = lane; e < need; e += 32)
+                tab[e] = __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
+            __syncwarp();
+        }
         // lane 0 streams Q and the K ring, lane 1 the V ring, so that a K
         // load never waits behind a V stage that frees later
         if (lane == 0) {
@@ -177,9 +240,8 @@ __global__ void __launch_bounds__(THREADS, 2)
                     break;
                 }
                 mbar_arrive_expect_tx(&bar->k_full[st], KV_BYTES);
-                for (int c = 0; c < 2; ++c)
-                    tma_load_3d(sbase + OFF_K + st * KV_BYTES + c * KBOX, &tm_k,
-                                &bar->k_full[st], 0, kvh * 2 + c, k0 + j * BN);
+                load_kv_tile<PAGED>(sbase + OFF_K + st * KV_BYTES, &tm_k, &bar->k_full[st], a, b,
+                                    kvh, k0, kl, j, &bar->bad_block, tab);
             }
         } else if (lane == 1) {
             prefetch_tmap(&tm_v);
@@ -191,9 +253,8 @@ __global__ void __launch_bounds__(THREADS, 2)
                     break;
                 }
                 mbar_arrive_expect_tx(&bar->v_full[st], KV_BYTES);
-                for (int c = 0; c < 2; ++c)
-                    tma_load_3d(sbase + OFF_V + st * KV_BYTES + c * KBOX, &tm_v,
-                                &bar->v_full[st], 0, kvh * 2 + c, k0 + j * BN);
+                load_kv_tile<PAGED>(sbase + OFF_V + st * KV_BYTES, &tm_v, &bar->v_full[st], a, b,
+                                    kvh, k0, kl, j, &bar->bad_block, tab);
             }
         }
         __syncwarp();
@@ -358,18 +419,27 @@ __global__ void __launch_bounds__(THREADS, 2)
     __syncthreads();
     tc_fence_after();
     if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (PAGED) {
+        // a needed block was missing: flag it and zero the tile's rows
+        if (bar->bad_block) {
+            if (tid == 0) flag_error(a.dev_err, PA_DEVERR_BAD_BLOCK);
+            if (tid < rows_here) {
+                uint4 *o = reinterpret_cast<uint4 *>(out + ((size_t)(q0 + m * BM + tid) * a.num_heads + h) * HD);
+                for (int c = 0; c < HD / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
 }
 
-}  // namespace
-
-int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                       const CUtensorMap &tm_v, cudaStream_t s)
+template <bool PAGED>
+int launch_varlen(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                  const CUtensorMap &tm_v, cudaStream_t s)
 {
     if (a.head_dim != HD) return PA_ERR_UNSUPPORTED;
     if (a.max_q <= 0) return PA_OK;
-    static bool attr_set = false;
+    static bool attr_set = false; // one process-wide attribute per kernel
     if (!attr_set) {
-        if (cudaFuncSetAttribute(varlen_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(varlen_tc_kernel<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES) != cudaSuccess)
             return PA_ERR_LAUNCH;
         attr_set = true;
@@ -377,8 +447,22 @@ int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUten
     const unsigned tiles = (unsigned)((a.max_q + BM - 1) / BM);
     if (tiles > 65535u || a.batch > 65535) return PA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)a.num_heads, tiles, (unsigned)a.batch);
-    varlen_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tm_q, tm_k, tm_v, a);
+    varlen_tc_kernel<PAGED><<<grid, THREADS, SMEM_BYTES, s>>>(tm_q, tm_k, tm_v, a);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                       const CUtensorMap &tm_v, cudaStream_t s)
+{
+    return launch_varlen<false>(a, tm_q, tm_k, tm_v, s);
+}
+
+int varlen_paged_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q,
+                             const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t s)
+{
+    return launch_varlen<true>(a, tm_q, tm_k, tm_v, s);
 }
 
 }  // namespace pa

@@ -1,0 +1,92 @@
+"""GPU parity of pa_varlen_paged: keys read through the block table from the
+pool.  Checked bit for bit against pa_cache_update (gather) + pa_varlen on the
+same inputs, and within tolerance against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_300_gb300 as pa
+from tests.gpu_util import assert_close, bits
+from workloads import make_varlen, to_numpy, varlen_config
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _needs_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pa.load()
+
+
+def _both_paths(c, causal=True, err=None):
+    """(fused output, gather + varlen output, gathered k, gathered v)."""
+    t = lambda x: x.to("cuda")
+    kc, vc = t(c.k_cache), t(c.v_cache)
+    cq, ck, pl, bt = t(c.cu_seq_lens_q), t(c.cu_seq_lens_k), t(c.prefix_lens), t(c.block_table)
+    q, kch, vch = t(c.q), t(c.k_chunk), t(c.v_chunk)
+    tk = int(c.cu_seq_lens_k[-1])
+    kf = torch.empty(tk, *c.k_chunk.shape[1:], dtype=c.k_chunk.dtype, device="cuda")
+    vf = torch.empty_like(kf)
+    pa.pa_cache_update(kch, vch, cq, pl, bt, kc, vc, kf, vf, ck)  # scatter + gather
+    seqlens_k = (c.cu_seq_lens_k[1:] - c.cu_seq_lens_k[:-1]).to(torch.int32).cuda()
+    fused = pa.pa_varlen_paged(q, kc, vc, bt, cq, seqlens_k, c.max_length_q, c.max_length_k,
+                               causal, dev_err=err)
+    ref = pa.pa_varlen(q, kf, vf, cq, ck, c.max_length_q, c.max_length_k, causal)
+    torch.cuda.synchronize()
+    return fused, ref, kf, vf
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
+@pytest.mark.parametrize("causal", [True, False])
+def test_paged_equals_gather_path_bitwise(bs, causal):
+    c = make_varlen(5 + bs, [1, 129, 300, 64, 255, 7, 0], [0, 17, 300, 5, 130, 513, 40], 8, 2,
+                    128, bs, causal=causal)
+    fused, ref, kf, vf = _both_paths(c, causal)
+    assert torch.equal(fused.view(torch.int16), ref.view(torch.int16))
+    o = oracle.varlen(to_numpy(c.q), bits(kf), bits(vf), c.cu_seq_lens_q.numpy(),
+                      c.cu_seq_lens_k.numpy(), causal)
+    assert_close(fused, o, torch.bfloat16, f"paged varlen bs={bs}")
+
+
+def test_paged_workload_scaled_against_oracle():
+    c = varlen_config(4, scale_down=8)
+    fused, ref, kf, vf = _both_paths(c)
+    assert torch.equal(fused.view(torch.int16), ref.view(torch.int16))
+    o = oracle.varlen(to_numpy(c.q), bits(kf), bits(vf), c.cu_seq_lens_q.numpy(),
+                      c.cu_seq_lens_k.numpy(), True)
+    assert_close(fused, o, torch.bfloat16, "paged varlen, workload 4 scaled")
+
+
+def test_paged_invariant_to_block_placement():
+    c = make_varlen(9, [200, 70], [100, 300], 8, 2, 128, 16)
+    g = torch.Generator().manual_seed(3)
+    nb = c.k_cache.shape[0]
+    pi = torch.randperm(nb, generator=g)
+    inv = torch.empty_like(pi)
+    inv[pi] = torch.arange(nb)
+    c2 = make_varlen(9, [200, 70], [100, 300], 8, 2, 128, 16)
+    c2.k_cache = c.k_cache[inv].clone()
+    c2.v_cache = c.v_cache[inv].clone()
+    m = c.block_table >= 0
+    c2.block_table = c.block_table.clone()
+    c2.block_table[m] = pi[c.block_table[m].long()].to(torch.int32)
+    a, _, _, _ = _both_paths(c)
+    b, _, _, _ = _both_paths(c2)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_paged_missing_block_flags_and_zeroes():
+    c = make_varlen(4, [50, 60], [100, 20], 8, 2, 128, 16)
+    c.block_table[0, 2] = -1  # a needed block of request 0 (positions 32..47)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t = lambda x: x.to("cuda")
+    seqlens_k = (c.cu_seq_lens_k[1:] - c.cu_seq_lens_k[:-1]).to(torch.int32)
+    out = pa.pa_varlen_paged(t(c.q), t(c.k_cache), t(c.v_cache), t(c.block_table),
+                             t(c.cu_seq_lens_q), t(seqlens_k), c.max_length_q, c.max_length_k,
+                             True, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.DEVERR_BAD_BLOCK
+    assert torch.all(out[:50] == 0)
+    assert not torch.all(out[50:] == 0)
