@@ -501,6 +501,18 @@ def main(argv=None):
             extra[key] = leg_summary(c, r["ms"], peaks)
             del r, c
             torch.cuda.empty_cache()
+        # paging overhead: the main workload again with every sequence's blocks
+        # adjacent in the pool (the layout of a non-paged cache), same kernel
+        c = decode_config(2, seed_offset=dist.rank, contiguous=True)
+        r = run_decode_leg(torch, pa, c, min(args.steps, 20), args.warmup, flush)
+        cms = sum(r["ms"]) / len(r["ms"])
+        extra["paging_overhead"] = {
+            "workload": c.name,
+            "contiguous_ms": round(cms, 5), "scattered_ms": round(ms, 5),
+            "scattered_over_contiguous": round(ms / cms, 4),
+            "note": "same kernel and data; only the physical placement of the blocks differs"}
+        del r, c
+        torch.cuda.empty_cache()
         vc = varlen_config(4)
         try:
             upd_ms, att_ms, scat_ms, patt_ms = run_varlen_leg(torch, pa, vc, min(args.steps, 20),

@@ -1,5 +1,6 @@
 """Build the CUDA library in-tree: nvcc, sm_103a only, one object per .cu
-(compiled in parallel), linked into ``_lib/libpa300.so``.
+(and per host-only .cpp), compiled in parallel, linked into
+``_lib/libpa300.so``.
 
 Run ``python -m paged_kv_cache_300_gb300._build`` or call ``build()``.
 """
@@ -32,12 +33,12 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(
-        os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "pa.h")]
+        os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
 def up_to_date() -> bool:

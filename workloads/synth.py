@@ -135,11 +135,15 @@ class DecodeCase:
         return c
 
 
-def _place_blocks(gen, need, num_blocks, shared=None):
+def _place_blocks(gen, need, num_blocks, shared=None, contiguous=False):
     """Assign physical blocks: a seeded random permutation of the pool,
-    handed out in order.  `shared` (list of physical ids) are reserved and
-    given to rows flagged in need as (shared_count, private_count)."""
+    handed out in order (or, with `contiguous`, the pool in order, so each
+    sequence's blocks are adjacent, as a non-paged cache would lay them out).
+    `shared` (list of physical ids) are reserved and given to rows flagged in
+    need as (shared_count, private_count)."""
     perm = torch.randperm(num_blocks, generator=gen).tolist()
+    if contiguous:
+        perm = list(range(num_blocks))
     if shared:
         reserved = set(shared)
         perm = [p for p in perm if p not in reserved]
@@ -165,7 +169,7 @@ def make_decode(seed: int, lengths, num_heads: int, num_kv_heads: int, head_dim:
                 block_size: int, dtype=torch.bfloat16, value_scale: float = 1.0,
                 slack: float = 0.1, shared_prefix_blocks: int = 0, shared_rows=None,
                 max_blocks_per_seq: int | None = None, block_table=None, num_blocks=None,
-                name: str = "") -> DecodeCase:
+                name: str = "", contiguous: bool = False) -> DecodeCase:
     """Decode case with cached lengths `lengths` (keys before the append).
 
     Without an explicit `block_table`, row b gets ceil((L_b + 1) / bs)
@@ -187,7 +191,7 @@ def make_decode(seed: int, lengths, num_heads: int, num_kv_heads: int, head_dim:
         shared = None
         if shared_rows and shared_prefix_blocks:
             shared = torch.randperm(nb, generator=gen)[:shared_prefix_blocks].tolist()
-        rows = _place_blocks(gen, need, nb, shared)
+        rows = _place_blocks(gen, need, nb, shared, contiguous)
         mb = max_blocks_per_seq or max(len(r) for r in rows)
         table = _table_tensor(rows, mb)
     else:
@@ -276,7 +280,8 @@ WORKED_EXAMPLE_TABLE = [[2, -1, -1, -1], [0, 1, -1, -1], [3, 5, 6, -1]]
 WORKED_EXAMPLE_SEQLENS = [30, 32, 70]
 
 
-def decode_config(idx: int, scale_down: int = 1, seed_offset: int = 0) -> DecodeCase:
+def decode_config(idx: int, scale_down: int = 1, seed_offset: int = 0,
+                  contiguous: bool = False) -> DecodeCase:
     """Decode workloads 1, 2, 3 and 5.  `scale_down` > 1 keeps the structure
     (heads, head_dim, block size, length distribution) with fewer sequences,
     for oracle runs that must finish in seconds.  `seed_offset` draws another
@@ -291,13 +296,15 @@ def decode_config(idx: int, scale_down: int = 1, seed_offset: int = 0) -> Decode
         b = max(1, 64 // scale_down)
         lengths = torch.randint(512, 4097, (b,), generator=g).tolist()
         return make_decode(seed, lengths, 32, 8, 128, 16, value_scale=1.0 / math.sqrt(128.0),
-                           name=CONFIG_NAMES[2])
+                           name=CONFIG_NAMES[2] + (" (blocks contiguous)" if contiguous else ""),
+                           contiguous=contiguous)
     if idx == 3:
         b = max(1, 256 // scale_down)
         z = torch.randn(b, generator=g, dtype=torch.float64)
         lengths = torch.exp(math.log(2048.0) + 1.0 * z).round().clamp(64, 32768)
         return make_decode(seed, lengths.to(torch.int64).tolist(), 64, 8, 128, 16,
-                           name=CONFIG_NAMES[3])
+                           name=CONFIG_NAMES[3] + (" (blocks contiguous)" if contiguous else ""),
+                           contiguous=contiguous)
     if idx == 5:
         n_short = max(1, 1024 // scale_down)
         n_long = 4 if scale_down == 1 else 1
