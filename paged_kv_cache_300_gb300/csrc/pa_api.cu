@@ -55,6 +55,35 @@ int encode_rows_map(CUtensorMap *map, const void *base, uint64_t rows, int heads
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_LAUNCH;
 }
 
+// 4-D bf16 view of q [rows, heads, 128] as (64 dims, 2 halves, heads, rows);
+// one box is one 64-dim half of `pack` consecutive heads for `box_queries`
+// consecutive rows, landing in shared memory as box_queries * pack rows of
+// 128 bytes (query-major, head-minor), 128-byte swizzled.
+int encode_packed_q_map(CUtensorMap *map, const void *base, uint64_t rows, int heads, int pack,
+                        int box_queries)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr) return PA_ERR_DEVICE;
+    const cuuint64_t dims[4] = {64, 2, (cuuint64_t)heads, rows};
+    const cuuint64_t strides[3] = {128, 256, (cuuint64_t)heads * 256};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)pack, (cuuint32_t)box_queries};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_LAUNCH;
+}
+
+// Query heads packed into one 128-row tile: the largest power of two that
+// divides the GQA group size (the heads of a tile then share one kv head).
+int varlen_pack_factor(int num_heads, int num_kv_heads)
+{
+    const int g = num_heads / num_kv_heads;
+    int p = 1;
+    while (p * 2 <= 128 && g % (p * 2) == 0) p *= 2;
+    return p;
+}
+
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace pa
@@ -234,8 +263,9 @@ int pa_varlen(const void *q, const void *k, const void *v, const int32_t *cu_seq
     if (head_dim != 128) return PA_ERR_UNSUPPORTED;
     CUtensorMap tm_q, tm_k, tm_v;
     int rc;
-    if ((rc = encode_rows_map(&tm_q, q, (uint64_t)total_q, num_heads, head_dim, kVarlenQRows)) !=
-        PA_OK)
+    a.pack = varlen_pack_factor(num_heads, num_kv_heads);
+    if ((rc = encode_packed_q_map(&tm_q, q, (uint64_t)total_q, num_heads, a.pack,
+                                  kVarlenQRows / a.pack)) != PA_OK)
         return rc;
     if (total_k > 0) {
         if ((rc = encode_rows_map(&tm_k, k, (uint64_t)total_k, num_kv_heads, head_dim,
@@ -294,8 +324,9 @@ int pa_varlen_paged(const void *q, const void *k_cache, const void *v_cache,
     CUtensorMap tm_q, tm_k, tm_v;
     int rc;
     const uint64_t rows = (uint64_t)num_blocks * block_size;
-    if ((rc = encode_rows_map(&tm_q, q, (uint64_t)total_q, num_heads, head_dim, kVarlenQRows)) !=
-        PA_OK)
+    a.pack = varlen_pack_factor(num_heads, num_kv_heads);
+    if ((rc = encode_packed_q_map(&tm_q, q, (uint64_t)total_q, num_heads, a.pack,
+                                  kVarlenQRows / a.pack)) != PA_OK)
         return rc;
     if ((rc = encode_rows_map(&tm_k, k_cache, rows, num_kv_heads, head_dim, block_size)) != PA_OK)
         return rc;

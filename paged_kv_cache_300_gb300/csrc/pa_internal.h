@@ -90,6 +90,9 @@ struct VarlenArgs {
     const int32_t *block_table;
     const int32_t *seqlens_k;
     int num_blocks, block_size, max_blocks_per_seq;
+    // tensor-core kernel: query heads packed per 128-row tile (a power of two
+    // dividing num_heads / num_kv_heads); a tile holds 128 / pack queries
+    int pack;
 };
 // Rows of one TMA box of the tensor-core varlen kernel: query tiles are 128
 // rows, key/value tiles 64 rows.
@@ -105,5 +108,8 @@ int varlen_paged_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q,
 int num_sms();
 int encode_rows_map(CUtensorMap *map, const void *base, uint64_t rows, int heads, int head_dim,
                     int box_rows);
+int encode_packed_q_map(CUtensorMap *map, const void *base, uint64_t rows, int heads, int pack,
+                        int box_queries);
+int varlen_pack_factor(int num_heads, int num_kv_heads);
 
 }  // namespace pa

@@ -5,10 +5,15 @@
 // query i of request r (lengths ql, kl) attends key j (j <= i + kl - ql when
 // causal), softmax(q k^T * scale) v; a query with no visible key gives 0.
 //
-// One CTA per (query head, 128-row query tile, request); grid.x runs over the
-// heads so the CTAs of one GQA group, which read the same K/V tiles, run
-// side by side and share them through L2.  Query tiles are issued from the
-// last (most keys under the causal mask) to the first.
+// One CTA per (group of `pack` query heads, 128-row tile, request).  The
+// rows of a tile are (query, head) pairs, query-major: the `pack` heads of one
+// GQA group (the largest power of two dividing the group size) times
+// 128 / pack consecutive queries, loaded by one 4-D TMA box per 64-dim half
+// (the heads of a query are adjacent in memory).  All rows of a tile use the
+// same kv head, so every K/V tile feeds 128 rows, while the ragged last tile
+// of a request and the causal diagonal band shrink by `pack`.  grid.x runs
+// over the head groups so the CTAs of one GQA group run side by side.  Tiles
+// are issued from the last (most keys under the causal mask) to the first.
 //
 // Warp roles (192 threads; two CTAs share an SM, 96 KB of shared memory and
 // 256 TMEM columns each, so one CTA's softmax overlaps the other's MMAs):
@@ -72,8 +77,9 @@ struct Barriers {
     uint64_t k_empty[NSTAGE];
     uint64_t v_empty[NSTAGE];
     uint64_t s_full[2];
-    uint64_t p_full;
-    uint64_t o_done;
+    uint64_t p_full[2];
+    uint64_t o_done;   // one phase per PV_j (waited only before an O rescale)
+    uint64_t all_done; // one phase: every MMA of the CTA has completed
     uint32_t tmem_base;
     int bad_block; // paged variant: a needed table entry was not a valid block
 };
@@ -151,17 +157,20 @@ __global__ void __launch_bounds__(THREADS, 2)
     const uint32_t sbase = smem_u32(smem);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x, b = blockIdx.z;
+    // tile rows are (query, head) pairs, query-major: `pack` query heads of
+    // one GQA group times QPT consecutive queries
+    const int pack = a.pack, QPT = BM / pack;
+    const int h0 = blockIdx.x * pack, b = blockIdx.z;
     const int m = gridDim.y - 1 - blockIdx.y; // heavy (late) tiles first
-    const int G = a.num_heads / a.num_kv_heads, kvh = h / G;
+    const int G = a.num_heads / a.num_kv_heads, kvh = h0 / G;
 
     const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
     int k0 = 0, kl = 0;
-    bool bad_cu = q0 < 0 || q1 < q0 || q1 > a.total_q || q1 - q0 > (int)gridDim.y * BM;
+    bool bad_cu = q0 < 0 || q1 < q0 || q1 > a.total_q || q1 - q0 > (int)gridDim.y * QPT;
     if constexpr (PAGED) {
         kl = __ldg(a.seqlens_k + b);
         if (kl < 0 || (long long)kl > (long long)a.max_blocks_per_seq * a.block_size) {
-            if (tid == 0 && h == 0 && m == 0) flag_error(a.dev_err, PA_DEVERR_OVERFLOW);
+            if (tid == 0 && h0 == 0 && m == 0) flag_error(a.dev_err, PA_DEVERR_OVERFLOW);
             kl = 0; // no keys: the rows below come out as zeros
         }
     } else {
@@ -171,20 +180,26 @@ __global__ void __launch_bounds__(THREADS, 2)
         kl = k1 - k0;
     }
     if (bad_cu) {
-        if (tid == 0 && h == 0 && m == 0) flag_error(a.dev_err, PA_DEVERR_BAD_CU);
+        if (tid == 0 && h0 == 0 && m == 0) flag_error(a.dev_err, PA_DEVERR_BAD_CU);
         return;
     }
     const int ql = q1 - q0;
-    if (m * BM >= ql) return;
-    const int rows_here = min(BM, ql - m * BM);
+    const int r0 = m * QPT; // first query of the tile inside the request
+    if (r0 >= ql) return;
+    const int qrows = min(QPT, ql - r0);
+    const int rows_here = qrows * pack; // valid tile rows
     int n_keys = kl;
-    if (a.causal) n_keys = max(0, min(kl, m * BM + rows_here - 1 + kl - ql + 1));
+    if (a.causal) n_keys = max(0, min(kl, r0 + qrows - 1 + kl - ql + 1));
     const int n_tiles = (n_keys + BN - 1) / BN;
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+    // output row of tile row r
+    auto out_row = [&](int r) -> size_t {
+        return ((size_t)(q0 + r0 + r / pack) * a.num_heads + h0 + r % pack) * HD;
+    };
 
     if (n_tiles == 0) { // no visible key for any row of the tile
         if (tid < rows_here) {
-            uint4 *o = reinterpret_cast<uint4 *>(out + ((size_t)(q0 + m * BM + tid) * a.num_heads + h) * HD);
+            uint4 *o = reinterpret_cast<uint4 *>(out + out_row(tid));
 #pragma unroll
             for (int c = 0; c < HD / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -201,8 +216,10 @@ __global__ void __launch_bounds__(THREADS, 2)
         }
         mbar_init(&bar->s_full[0], 1);
         mbar_init(&bar->s_full[1], 1);
-        mbar_init(&bar->p_full, 4);
+        mbar_init(&bar->p_full[0], 4);
+        mbar_init(&bar->p_full[1], 4);
         mbar_init(&bar->o_done, 1);
+        mbar_init(&bar->all_done, 1);
         bar->bad_block = 0;
         fence_mbar_init();
     }
@@ -230,8 +247,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             prefetch_tmap(&tm_k);
             mbar_arrive_expect_tx(&bar->q_full, Q_BYTES);
             for (int c = 0; c < 2; ++c)
-                tma_load_3d(sbase + OFF_Q + c * QBOX, &tm_q, &bar->q_full, 0, h * 2 + c,
-                            q0 + m * BM);
+                tma_load_4d(sbase + OFF_Q + c * QBOX, &tm_q, &bar->q_full, 0, c, h0, q0 + r0);
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j & 1;
                 // K_j's stage frees when S_{j-2} has been computed
@@ -286,7 +302,8 @@ __global__ void __launch_bounds__(THREADS, 2)
             if (ok && n_tiles > 1) ok = issue_qk(1);
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const int st = j & 1;
-                if (!mbar_wait(&bar->p_full, j & 1) || !mbar_wait(&bar->v_full[st], (j >> 1) & 1)) {
+                if (!mbar_wait(&bar->p_full[st], (j >> 1) & 1) ||
+                    !mbar_wait(&bar->v_full[st], (j >> 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -302,6 +319,10 @@ __global__ void __launch_bounds__(THREADS, 2)
                 umma_commit(&bar->v_empty[st]);
                 if (j + 2 < n_tiles && !(ok = issue_qk(j + 2))) break;
             }
+            if (ok) umma_commit(&bar->all_done); // tracks every MMA issued above
+            // and the last o_done arrival lands before the CTA leaves (every
+            // MMA is complete once all_done is, so the parity is unambiguous)
+            if (ok) ok = mbar_wait(&bar->all_done, 0) && mbar_wait(&bar->o_done, (n_tiles - 1) & 1);
             // the producer never waits for the last two stage releases: wait
             // here so that no commit arrives after the CTA has left
             for (int t = max(0, n_tiles - 2); t < n_tiles && ok; ++t)
@@ -312,7 +333,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     } else {
         // ================= softmax: thread r <-> query row r =================
         const int r = tid;
-        const int i = m * BM + r; // row inside the request
+        const int i = r0 + r / pack; // query of this row inside the request
         const int lim = a.causal ? min(i + kl - ql, kl - 1) : kl - 1; // last visible key
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         const float sl2 = a.scale_log2;
@@ -367,13 +388,20 @@ __global__ void __launch_bounds__(THREADS, 2)
             // P row (bf16 pairs) over the S_j row it came from; PV_j reads it
             // as the TMEM A operand.  Its own buffer: no wait on PV_{j-1}.
             tmem_st32(trow + st * BN, pk);
-            if (j > 0) { // PV_{j-1} must be done before O is rescaled and P_j released
+            // O is rescaled only by a warp with a row whose max grew past the
+            // threshold, after PV_{j-1} is done and before PV_j (which needs
+            // this warp's arrival).  Otherwise P_j is released at once and
+            // PV_j queues behind PV_{j-1} without a round trip.
+            // (S_j being ready implies PV_{j-2} is done -- its commit covers
+            // every earlier MMA -- so o_done is at most one phase behind and
+            // its parity is unambiguous)
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
                 if (!mbar_wait(&bar->o_done, (j - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, need)) {
+                {
 #pragma unroll
                     for (int c = 0; c < HD / 32; ++c) {
                         uint32_t o[32];
@@ -389,12 +417,14 @@ __global__ void __launch_bounds__(THREADS, 2)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->p_full);
+            if (lane == 0) mbar_arrive(&bar->p_full[st]);
         }
-        if (ok && mbar_wait(&bar->o_done, (n_tiles - 1) & 1)) {
+        // two PVs may still be in flight here, so the epilogue waits on the
+        // single-phase barrier committed after the last one
+        if (ok && mbar_wait(&bar->all_done, 0)) {
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            uint4 *orow = reinterpret_cast<uint4 *>(out + ((size_t)(q0 + i) * a.num_heads + h) * HD);
+            uint4 *orow = reinterpret_cast<uint4 *>(out + out_row(r));
 #pragma unroll
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
@@ -424,7 +454,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         if (bar->bad_block) {
             if (tid == 0) flag_error(a.dev_err, PA_DEVERR_BAD_BLOCK);
             if (tid < rows_here) {
-                uint4 *o = reinterpret_cast<uint4 *>(out + ((size_t)(q0 + m * BM + tid) * a.num_heads + h) * HD);
+                uint4 *o = reinterpret_cast<uint4 *>(out + out_row(tid));
                 for (int c = 0; c < HD / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
@@ -444,9 +474,10 @@ int launch_varlen(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMa
             return PA_ERR_LAUNCH;
         attr_set = true;
     }
-    const unsigned tiles = (unsigned)((a.max_q + BM - 1) / BM);
+    const int qpt = BM / a.pack;
+    const unsigned tiles = (unsigned)((a.max_q + qpt - 1) / qpt);
     if (tiles > 65535u || a.batch > 65535) return PA_ERR_UNSUPPORTED;
-    dim3 grid((unsigned)a.num_heads, tiles, (unsigned)a.batch);
+    dim3 grid((unsigned)(a.num_heads / a.pack), tiles, (unsigned)a.batch);
     varlen_tc_kernel<PAGED><<<grid, THREADS, SMEM_BYTES, s>>>(tm_q, tm_k, tm_v, a);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }
