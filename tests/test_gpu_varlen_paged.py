@@ -90,3 +90,39 @@ def test_paged_missing_block_flags_and_zeroes():
     assert int(err.item()) & pa.DEVERR_BAD_BLOCK
     assert torch.all(out[:50] == 0)
     assert not torch.all(out[50:] == 0)
+
+
+def test_mixed_decode_and_prefill_in_one_launch():
+    """A continuous-batching step: decode requests (one new token) and
+    prefill chunks together, scattered with pa_cache_update and attended by
+    one pa_varlen_paged launch.  Decode rows match pa_decode on the same
+    state; every row matches the oracle."""
+    q_lens = [1, 200, 1, 1, 57, 1]
+    prefix = [300, 0, 17, 130, 400, 0]
+    c = make_varlen(21, q_lens, prefix, 8, 2, 128, 16)
+    t = lambda x: x.to("cuda")
+    kc, vc = t(c.k_cache), t(c.v_cache)
+    kc0, vc0 = kc.clone(), vc.clone()
+    cq, bt, pl = t(c.cu_seq_lens_q), t(c.block_table), t(c.prefix_lens)
+    q, kch, vch = t(c.q), t(c.k_chunk), t(c.v_chunk)
+    pa.pa_cache_update(kch, vch, cq, pl, bt, kc, vc)
+    seqlens_k = (c.cu_seq_lens_k[1:] - c.cu_seq_lens_k[:-1]).to(torch.int32).cuda()
+    mixed = pa.pa_varlen_paged(q, kc, vc, bt, cq, seqlens_k, c.max_length_q, c.max_length_k, True)
+    torch.cuda.synchronize()
+    # the oracle on the gathered keys
+    kf, vf = oracle.cache_update(to_numpy(c.k_chunk), to_numpy(c.v_chunk), c.cu_seq_lens_q.numpy(),
+                                 c.prefix_lens.numpy(), c.block_table.numpy(),
+                                 to_numpy(c.k_cache).copy(), to_numpy(c.v_cache).copy(),
+                                 c.cu_seq_lens_k.numpy())
+    ref = oracle.varlen(to_numpy(c.q), kf, vf, c.cu_seq_lens_q.numpy(), c.cu_seq_lens_k.numpy(),
+                        True)
+    assert_close(mixed, ref, torch.bfloat16, "mixed batch")
+    # decode rows through the decode kernel on the pre-step pool
+    dec = [r for r, n in enumerate(q_lens) if n == 1]
+    rows = c.cu_seq_lens_q[dec].long()
+    out_d = pa.pa_decode(q[rows.cuda()].contiguous(), kc0, vc0, bt[dec].contiguous(),
+                         pl[dec].contiguous(), kch[rows.cuda()].contiguous(),
+                         vch[rows.cuda()].contiguous())
+    torch.cuda.synchronize()
+    assert_close(out_d, mixed[rows.cuda()].double().cpu().numpy(), torch.bfloat16,
+                 "decode kernel vs mixed launch")
