@@ -13,9 +13,10 @@
 namespace pa {
 
 // Upper bound on polls of one mbarrier phase before a wait gives up.  Each
-// poll is an mbarrier.try_wait, which itself suspends for a while, so this is
-// seconds of wall time: far beyond any legitimate wait, short enough that a
-// broken pipeline returns with PA_DEVERR_TIMEOUT instead of hanging.
+// poll is an mbarrier.try_wait that suspends for up to kWaitSuspendNs, so
+// this is at most a few seconds of wall time: far beyond any legitimate
+// wait, short enough that a broken pipeline returns with PA_DEVERR_TIMEOUT
+// instead of hanging.
 constexpr uint32_t kWaitPolls = 1u << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -52,15 +53,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// One poll: suspends the thread for at most kWaitSuspendNs while the phase
+// is incomplete.  Without the hint the suspension lasts a system-defined
+// slice that measured far longer than a pipeline hand-off on GB300 (the
+// tensor-core varlen kernel ran 9% slower), so every poll names a short one.
+constexpr uint32_t kWaitSuspendNs = 256;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitSuspendNs)
         : "memory");
     return ok != 0;
 }

@@ -64,8 +64,13 @@ constexpr int OFF_V = OFF_K + NSTAGE * KV_BYTES;
 constexpr int OFF_BAR = OFF_V + NSTAGE * KV_BYTES;
 constexpr int TAB_CAP = 512;                  // block-table entries staged in smem (paged)
 constexpr int OFF_TAB = OFF_BAR + 256;
-constexpr int SMEM_BYTES = OFF_TAB + 4 * TAB_CAP + 1024; // + alignment slack: two CTAs per SM
-constexpr int THREADS = 192;
+// two staged copies of the table slice (one per loader warp), + alignment
+// slack: still two CTAs per SM
+constexpr int SMEM_BYTES = OFF_TAB + 2 * 4 * TAB_CAP + 1024;
+// warps 0-3 softmax, 4 TMA (Q + K; contiguous keys: V too), 5 MMA; paged
+// keys take one box per block, so the V loader gets warp 6 of its own and
+// neither ring waits behind the other's issue loop
+template <bool PAGED> constexpr int kThreads = PAGED ? 224 : 192;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t COL_O = 2 * BN;
 constexpr float kRescaleThreshold = 8.0f; // log2 units
@@ -146,7 +151,7 @@ __device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap *ma
 }
 
 template <bool PAGED>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(kThreads<PAGED>, 2)
     varlen_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const VarlenArgs a)
 {
@@ -230,9 +235,10 @@ __global__ void __launch_bounds__(THREADS, 2)
     const uint32_t tmem = bar->tmem_base;
     bool ok = true;
 
-    if (warp == 4) {
+    if (warp == 4 || warp == 6) {
         // ================= TMA producers =================
-        int *tab = reinterpret_cast<int *>(smem + OFF_TAB);
+        // each loader warp stages its own copy of the table slice
+        int *tab = reinterpret_cast<int *>(smem + OFF_TAB + (warp == 6 ? 4 * TAB_CAP : 0));
         if constexpr (PAGED) {
             // stage this CTA's slice of the block table (coalesced, once)
             const int need = min(TAB_CAP, (min(kl, n_tiles * BN) + a.block_size - 1) / a.block_size);
@@ -240,9 +246,11 @@ __global__ void __launch_bounds__(THREADS, 2)
                 tab[e] = __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
             __syncwarp();
         }
-        // lane 0 streams Q and the K ring, lane 1 the V ring, so that a K
-        // load never waits behind a V stage that frees later
-        if (lane == 0) {
+        // one thread streams Q and the K ring, another the V ring, so that a
+        // K load never waits behind a V stage that frees later
+        const bool k_lane = warp == 4 && lane == 0;
+        const bool v_lane = PAGED ? (warp == 6 && lane == 0) : (warp == 4 && lane == 1);
+        if (k_lane) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             mbar_arrive_expect_tx(&bar->q_full, Q_BYTES);
@@ -259,7 +267,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                 load_kv_tile<PAGED>(sbase + OFF_K + st * KV_BYTES, &tm_k, &bar->k_full[st], a, b,
                                     kvh, k0, kl, j, &bar->bad_block, tab);
             }
-        } else if (lane == 1) {
+        } else if (v_lane) {
             prefetch_tmap(&tm_v);
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j & 1;
@@ -478,7 +486,7 @@ int launch_varlen(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMa
     const unsigned tiles = (unsigned)((a.max_q + qpt - 1) / qpt);
     if (tiles > 65535u || a.batch > 65535) return PA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)(a.num_heads / a.pack), tiles, (unsigned)a.batch);
-    varlen_tc_kernel<PAGED><<<grid, THREADS, SMEM_BYTES, s>>>(tm_q, tm_k, tm_v, a);
+    varlen_tc_kernel<PAGED><<<grid, kThreads<PAGED>, SMEM_BYTES, s>>>(tm_q, tm_k, tm_v, a);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }
 

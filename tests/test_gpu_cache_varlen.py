@@ -78,12 +78,14 @@ def test_cache_update_bad_cu_k_flags():
     assert int(err.item()) & pa.DEVERR_BAD_CU
 
 
-def _varlen_check(q, k, v, cu_q, cu_k, causal, dtype):
+def _varlen_check(q, k, v, cu_q, cu_k, causal, dtype, max_q=None):
     dev = "cuda"
     ql = np.diff(cu_q.numpy())
     kl = np.diff(cu_k.numpy())
+    if max_q is None:
+        max_q = int(ql.max()) if len(ql) else 0
     out = pa.pa_varlen(q.to(dev), k.to(dev), v.to(dev), cu_q.to(dev), cu_k.to(dev),
-                       int(ql.max()) if len(ql) else 0, int(kl.max()) if len(kl) else 0, causal)
+                       max_q, int(kl.max()) if len(kl) else 0, causal)
     torch.cuda.synchronize()
     ref = oracle.varlen(to_numpy(q), to_numpy(k), to_numpy(v), cu_q.numpy(), cu_k.numpy(), causal)
     return out, ref, assert_close(out, ref, dtype, f"varlen causal={causal}")
@@ -119,6 +121,45 @@ def test_varlen_ragged_tiles(causal, dtype):
     k = torch.randn(sum(kl), 2, 128, generator=gen).to(dtype)
     v = torch.randn(sum(kl), 2, 128, generator=gen).to(dtype)
     _varlen_check(q, k, v, cu_q, cu_k, causal, dtype)
+
+
+@pytest.mark.parametrize("heads", [(4, 4), (8, 4), (16, 2)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_pack_factors(heads, causal):
+    """GQA groups of 1, 2 and 8 query heads: 1, 2 and 8 heads share each
+    128-row tile."""
+    hq, hkv = heads
+    gen = torch.Generator().manual_seed(hq + hkv)
+    ql = [3, 200, 65, 1, 130]
+    kl = [40, 300, 65, 9, 129]
+    cu_q = torch.tensor([0] + list(np.cumsum(ql)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(np.cumsum(kl)), dtype=torch.int32)
+    q = torch.randn(sum(ql), hq, 128, generator=gen).to(torch.bfloat16)
+    k = torch.randn(sum(kl), hkv, 128, generator=gen).to(torch.bfloat16)
+    v = torch.randn(sum(kl), hkv, 128, generator=gen).to(torch.bfloat16)
+    _varlen_check(q, k, v, cu_q, cu_k, causal, torch.bfloat16)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_many_items(causal):
+    """Hundreds of short requests (some empty), a few long ones, and a
+    max_length_q far above the longest request: many more work items than
+    SMs, most of them empty, all taken over by the running CTAs."""
+    gen = torch.Generator().manual_seed(11)
+    rng = np.random.default_rng(11)
+    n = 400
+    ql = rng.integers(0, 6, n)
+    ql[[7, 150, 399]] = [600, 257, 1000]
+    kl = ql + rng.integers(0, 300, n)
+    kl[[20, 21]] = 0
+    ql[[20, 21]] = [0, 4]
+    cu_q = torch.tensor([0] + list(np.cumsum(ql)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(np.cumsum(kl)), dtype=torch.int32)
+    q = torch.randn(int(ql.sum()), 8, 128, generator=gen).to(torch.bfloat16)
+    k = torch.randn(int(kl.sum()), 2, 128, generator=gen).to(torch.bfloat16)
+    v = torch.randn(int(kl.sum()), 2, 128, generator=gen).to(torch.bfloat16)
+    out, _, _ = _varlen_check(q, k, v, cu_q, cu_k, causal, torch.bfloat16, max_q=4000)
+    assert torch.all(out[int(cu_q[21]):int(cu_q[22])] == 0)  # request 21 has no keys
 
 
 def test_varlen_workload_scaled():
