@@ -484,32 +484,70 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
                 last = __shfl_sync(kFull, last, 0);
                 if (last) {
                     __threadfence();
-                    // fold the partials in logical (CTA) order
-                    for (int g = 0; g < G; ++g) {
-                        float m = -INFINITY, l = 0.f, o[D / 32];
-                        bool anybad = false;
+                    // fold the partials in logical (CTA) order.  Each
+                    // partial's (m, l) and accumulator rows for every head of
+                    // the group are loaded together before any of them is
+                    // folded: one L2 round trip per partial instead of one
+                    // per (head, partial) -- this fold runs at the very end
+                    // of the launch, so its latency is the launch's tail.
+                    // Heads go in pairs (G <= 8, checked by the plan): 12 to
+                    // 20 loads in flight per round trip, and few enough
+                    // registers that the 9-warp variant (at most 168 per
+                    // thread) does not spill; chunks of 4 spilled there.
+                    constexpr int GC = 2, DL = D / 32;
+                    for (int gb = 0; gb < G; gb += GC) {
+                        float m[GC], l[GC], o[GC][DL];
+                        bool gbad[GC];
 #pragma unroll
-                        for (int k = 0; k < D / 32; ++k) o[k] = 0.f;
+                        for (int g = 0; g < GC; ++g) {
+                            m[g] = -INFINITY;
+                            l[g] = 0.f;
+                            gbad[g] = false;
+#pragma unroll
+                            for (int k = 0; k < DL; ++k) o[g][k] = 0.f;
+                        }
                         for (int k = 0; k < nseg; ++k) {
                             const int c = dense ? cfirst + k : cta_of(F + k, P, U);
                             const float *sc = a.part + (size_t)(c + segrow) * slot_floats;
-                            const float mc = __ldcg(sc + (size_t)HS * G * D + (hw * G + g) * 2);
-                            const float lc = __ldcg(sc + (size_t)HS * G * D + (hw * G + g) * 2 + 1);
-                            anybad |= lc < 0.f;
-                            const float mn = fmaxf(m, mc);
-                            const float mu = mn == -INFINITY ? 0.f : mn;
-                            const float wa = exp2_approx(m - mu), wb = exp2_approx(mc - mu);
-                            l = l * wa + lc * wb;
-                            const float *pc = sc + ((size_t)hw * G + g) * D;
+                            const float *ml = sc + (size_t)HS * G * D + ((size_t)hw * G + gb) * 2;
+                            const float *pc = sc + ((size_t)hw * G + gb) * D;
+                            float mc[GC], lc[GC], oc[GC][DL];
 #pragma unroll
-                            for (int k = 0; k < D / 32; ++k)
-                                o[k] = o[k] * wa + __ldcg(pc + lane + 32 * k) * wb;
-                            m = mn;
+                            for (int g = 0; g < GC; ++g) {
+                                if (gb + g < G) {
+                                    mc[g] = __ldcg(ml + g * 2);
+                                    lc[g] = __ldcg(ml + g * 2 + 1);
+#pragma unroll
+                                    for (int kk = 0; kk < DL; ++kk)
+                                        oc[g][kk] = __ldcg(pc + (size_t)g * D + lane + 32 * kk);
+                                }
+                            }
+#pragma unroll
+                            for (int g = 0; g < GC; ++g) {
+                                if (gb + g < G) {
+                                    gbad[g] |= lc[g] < 0.f;
+                                    const float mn = fmaxf(m[g], mc[g]);
+                                    const float mu = mn == -INFINITY ? 0.f : mn;
+                                    const float wa = exp2_approx(m[g] - mu);
+                                    const float wb = exp2_approx(mc[g] - mu);
+                                    l[g] = l[g] * wa + lc[g] * wb;
+#pragma unroll
+                                    for (int kk = 0; kk < DL; ++kk)
+                                        o[g][kk] = o[g][kk] * wa + oc[g][kk] * wb;
+                                    m[g] = mn;
+                                }
+                            }
                         }
-                        const float inv = (anybad || !(l > 0.f)) ? 0.f : 1.f / l;
 #pragma unroll
-                        for (int k = 0; k < D / 32; ++k)
-                            out[orow + (size_t)g * D + lane + 32 * k] = __float2bfloat16_rn(o[k] * inv);
+                        for (int g = 0; g < GC; ++g) {
+                            if (gb + g < G) {
+                                const float inv = (gbad[g] || !(l[g] > 0.f)) ? 0.f : 1.f / l[g];
+#pragma unroll
+                                for (int k = 0; k < DL; ++k)
+                                    out[orow + (size_t)(gb + g) * D + lane + 32 * k] =
+                                        __float2bfloat16_rn(o[g][k] * inv);
+                            }
+                        }
                     }
                     if (lane == 0) *ticket = 0;
                 }
