@@ -266,18 +266,33 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
     int stage = 0;
     uint32_t phase = 0;
 
+    // q fragments of the sequence after this one, fetched during this one's
+    // last unit so that a new segment does not start on a dependent load
+    uint32_t qn[Gm::KS][2];
+    bool qn_ok = false;
+    const int gq = lane >> 2;
+    auto load_q = [&](int b, int kvh_, uint32_t(&dst)[Gm::KS][2]) {
+        const __nv_bfloat16 *qrow = qp + ((size_t)b * Hq + (size_t)kvh_ * G + gq) * D + 2 * (lane & 3);
+#pragma unroll
+        for (int ks = 0; ks < Gm::KS; ++ks) {
+            dst[ks][0] = gq < G ? __ldg(reinterpret_cast<const unsigned int *>(qrow + ks * 16)) : 0u;
+            dst[ks][1] = gq < G ? __ldg(reinterpret_cast<const unsigned int *>(qrow + ks * 16 + 8)) : 0u;
+        }
+    };
+
     for (long long u = u0; u < u1; ++u) {
         const int kvh = w.hg * HS + hw;
         if (!open) {
-            const int gq = lane >> 2;
-            const __nv_bfloat16 *qrow =
-                qp + ((size_t)w.b * Hq + (size_t)kvh * G + gq) * D + 2 * (lane & 3);
+            if (qn_ok) {
 #pragma unroll
-            for (int ks = 0; ks < Gm::KS; ++ks) {
-                qf[ks][0] = gq < G ? __ldg(reinterpret_cast<const unsigned int *>(qrow + ks * 16)) : 0u;
-                qf[ks][1] =
-                    gq < G ? __ldg(reinterpret_cast<const unsigned int *>(qrow + ks * 16 + 8)) : 0u;
+                for (int ks = 0; ks < Gm::KS; ++ks) {
+                    qf[ks][0] = qn[ks][0];
+                    qf[ks][1] = qn[ks][1];
+                }
+            } else {
+                load_q(w.b, kvh, qf);
             }
+            qn_ok = false;
 #pragma unroll
             for (int i = 0; i < Gm::KS; ++i)
                 acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -286,6 +301,13 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
             bad = w.len < 0;
             seg_j0 = w.j;
             open = true;
+        }
+        if (w.j == w.nblk - 1 && u + 1 < u1) {
+            // the next unit starts sequence b + 1 (or sequence 0 of the next
+            // head group): its q is in flight while this unit is computed
+            const bool wrap = w.b + 1 == B;
+            load_q(wrap ? 0 : w.b + 1, (wrap ? w.hg + 1 : w.hg) * HS + hw, qn);
+            qn_ok = true;
         }
         if (!mbar_wait(&full[stage], phase)) {
             if (lane == 0) flag_error(a.dev_err, PA_DEVERR_TIMEOUT);
