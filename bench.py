@@ -52,8 +52,8 @@ def source_hash(name: str) -> str:
 # DRAM traffic per launch taken from ncu captures (profiles/), valid only for
 # the kernel source they were measured on.
 NCU_TRAFFIC = {
-    ("pa_decode.cu", "workload2"): {"src": "2036b8eb8d4720af", "bytes": 560_344_832},
-    ("pa_varlen_tc.cu", "workload4"): {"src": "632f1a59608846a4", "bytes": 662_209_024},
+    ("pa_decode.cu", "workload2"): {"src": "c7b4ab8baeb88746", "bytes": 560_410_880},
+    ("pa_varlen_tc.cu", "workload4"): {"src": "b52bf2f4e2292e5e", "bytes": 662_321_408},
 }
 
 
