@@ -57,11 +57,22 @@ constexpr int QBOX = BM * 128;                // 128 rows x 64 dims bf16, 128-by
 constexpr int KBOX = BN * 128;                // 64 keys x 64 dims
 constexpr int Q_BYTES = 2 * QBOX;             // the query tile: two 64-dim boxes
 constexpr int KV_BYTES = 2 * KBOX;            // one K (or V) tile of 64 keys
+// Key/value ring: stage i % 2 holds transaction T_i, T_0 = {K_0, K_1} and
+// T_i = {V_(i-1), K_(i+1)} for i >= 1: the V tile of P V_(i-1) and the K tile
+// of S_(i+1), which the MMA thread issues back to back.  One transaction of
+// two tiles instead of one per tile halves the TMA transactions per key (a
+// TMA transaction costs a few hundred cycles whatever its size, and the
+// per-tile rings kept the SM's TMA unit busy all the time).  Paged keys take
+// one box per block, so there the cost is per box, not per transaction, and
+// the same 64 KB hold a K ring and a V ring of two 16 KB stages each
+// (K_j's stage frees when S_j is done, V_j's when P V_j is): V tiles then go
+// out earlier than the K tiles of the same step and the two box streams do
+// not interleave.
 constexpr int NSTAGE = 2;
+constexpr int STAGE_BYTES = 2 * KV_BYTES;     // slot A (V, or K_0) + slot B (K)
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + Q_BYTES;
-constexpr int OFF_V = OFF_K + NSTAGE * KV_BYTES;
-constexpr int OFF_BAR = OFF_V + NSTAGE * KV_BYTES;
+constexpr int OFF_KV = OFF_Q + Q_BYTES;      // paged keys: K ring, then V ring
+constexpr int OFF_BAR = OFF_KV + NSTAGE * STAGE_BYTES;
 constexpr int TAB_CAP = 512;                  // block-table entries staged in smem (paged)
 constexpr int OFF_TAB = OFF_BAR + 256;
 // two staged copies of the table slice (one per loader warp), + alignment
@@ -77,9 +88,9 @@ constexpr float kRescaleThreshold = 8.0f; // log2 units
 
 struct Barriers {
     uint64_t q_full;
-    uint64_t k_full[NSTAGE];
-    uint64_t v_full[NSTAGE];
-    uint64_t k_empty[NSTAGE];
+    uint64_t kv_full[NSTAGE];  // the transaction (paged keys: the K ring)
+    uint64_t kv_empty[NSTAGE];
+    uint64_t v_full[NSTAGE];   // paged keys: the V ring
     uint64_t v_empty[NSTAGE];
     uint64_t s_full[2];
     uint64_t p_full[2];
@@ -214,9 +225,9 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
     if (tid == 0) {
         mbar_init(&bar->q_full, 1);
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&bar->k_full[s], 1);
+            mbar_init(&bar->kv_full[s], 1);
+            mbar_init(&bar->kv_empty[s], 1);
             mbar_init(&bar->v_full[s], 1);
-            mbar_init(&bar->k_empty[s], 1);
             mbar_init(&bar->v_empty[s], 1);
         }
         mbar_init(&bar->s_full[0], 1);
@@ -246,39 +257,67 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
                 tab[e] = __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
             __syncwarp();
         }
-        // one thread streams Q and the K ring, another the V ring, so that a
-        // K load never waits behind a V stage that frees later
+        // two threads load: one Q and the K tiles, the other the V tiles, so
+        // that neither waits behind the other's issue loop (contiguous keys:
+        // the K thread announces each transaction's bytes, V included)
         const bool k_lane = warp == 4 && lane == 0;
         const bool v_lane = PAGED ? (warp == 6 && lane == 0) : (warp == 4 && lane == 1);
-        if (k_lane) {
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            mbar_arrive_expect_tx(&bar->q_full, Q_BYTES);
-            for (int c = 0; c < 2; ++c)
-                tma_load_4d(sbase + OFF_Q + c * QBOX, &tm_q, &bar->q_full, 0, c, h0, q0 + r0);
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
-                // K_j's stage frees when S_{j-2} has been computed
-                if (j >= NSTAGE && !mbar_wait(&bar->k_empty[st], ((j >> 1) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&bar->k_full[st], KV_BYTES);
-                load_kv_tile<PAGED>(sbase + OFF_K + st * KV_BYTES, &tm_k, &bar->k_full[st], a, b,
-                                    kvh, k0, kl, j, &bar->bad_block, tab);
+        if (k_lane || v_lane) {
+            if (k_lane) {
+                prefetch_tmap(&tm_q);
+                prefetch_tmap(&tm_k);
+                mbar_arrive_expect_tx(&bar->q_full, Q_BYTES);
+                for (int c = 0; c < 2; ++c)
+                    tma_load_4d(sbase + OFF_Q + c * QBOX, &tm_q, &bar->q_full, 0, c, h0, q0 + r0);
+            } else {
+                prefetch_tmap(&tm_v);
             }
-        } else if (v_lane) {
-            prefetch_tmap(&tm_v);
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
-                // V_j's stage frees when PV_{j-2} is done
-                if (j >= NSTAGE && !mbar_wait(&bar->v_empty[st], ((j >> 1) - 1) & 1)) {
-                    ok = false;
-                    break;
+            if constexpr (PAGED) {
+                // K ring (K thread) or V ring (V thread): stage j % 2 holds
+                // tile j and frees when the MMAs reading tile j - 2 are done
+                uint64_t *full = k_lane ? bar->kv_full : bar->v_full;
+                uint64_t *empty = k_lane ? bar->kv_empty : bar->v_empty;
+                const uint32_t ring = sbase + OFF_KV + (k_lane ? 0 : NSTAGE * KV_BYTES);
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int st = j & 1;
+                    if (j >= NSTAGE && !mbar_wait(&empty[st], ((j >> 1) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[st], KV_BYTES);
+                    load_kv_tile<PAGED>(ring + st * KV_BYTES, k_lane ? &tm_k : &tm_v, &full[st], a,
+                                        b, kvh, k0, kl, j, &bar->bad_block, tab);
                 }
-                mbar_arrive_expect_tx(&bar->v_full[st], KV_BYTES);
-                load_kv_tile<PAGED>(sbase + OFF_V + st * KV_BYTES, &tm_v, &bar->v_full[st], a, b,
-                                    kvh, k0, kl, j, &bar->bad_block, tab);
+            } else {
+                for (int i = 0; i <= n_tiles; ++i) {
+                    const int st = i & 1;
+                    // T_i's stage frees when the MMAs reading T_(i-2) are done
+                    if (i >= NSTAGE && !mbar_wait(&bar->kv_empty[st], ((i >> 1) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t slot_a = sbase + OFF_KV + st * STAGE_BYTES;
+                    const uint32_t slot_b = slot_a + KV_BYTES;
+                    if (k_lane) {
+                        // announces the whole transaction: K tiles and V tile
+                        const int kb = i + 1; // K tile in slot B for i >= 1
+                        const int tiles = i == 0 ? min(2, n_tiles) : 1 + (kb < n_tiles ? 1 : 0);
+                        mbar_arrive_expect_tx(&bar->kv_full[st], tiles * KV_BYTES);
+                        if (i == 0) {
+                            load_kv_tile<PAGED>(slot_a, &tm_k, &bar->kv_full[st], a, b, kvh, k0, kl,
+                                                0, &bar->bad_block, tab);
+                            if (n_tiles > 1)
+                                load_kv_tile<PAGED>(slot_b, &tm_k, &bar->kv_full[st], a, b, kvh, k0,
+                                                    kl, 1, &bar->bad_block, tab);
+                        } else if (kb < n_tiles) {
+                            load_kv_tile<PAGED>(slot_b, &tm_k, &bar->kv_full[st], a, b, kvh, k0, kl,
+                                                kb, &bar->bad_block, tab);
+                        }
+                    } else if (i >= 1) {
+                        load_kv_tile<PAGED>(slot_a, &tm_v, &bar->kv_full[st], a, b, kvh, k0, kl,
+                                            i - 1, &bar->bad_block, tab);
+                    }
+                }
             }
         }
         __syncwarp();
@@ -289,53 +328,90 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
             constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, HD, 0, 1);
             const uint32_t qs = sbase + OFF_Q;
             ok = mbar_wait(&bar->q_full, 0);
-            auto issue_qk = [&](int j) -> bool {
-                const int st = j & 1;
-                if (!mbar_wait(&bar->k_full[st], (j >> 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t ks = sbase + OFF_K + st * KV_BYTES;
+            // S_j = Q K_j^T into S buffer j % 2, K_j read from `ks`
+            auto issue_qk = [&](int j, uint32_t ks) {
+                const int sb = j & 1;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
-                    umma_bf16(tmem + st * BN, kmajor_desc(qs, kk, QBOX), kmajor_desc(ks, kk, KBOX),
+                    umma_bf16(tmem + sb * BN, kmajor_desc(qs, kk, QBOX), kmajor_desc(ks, kk, KBOX),
                               idesc_qk, kk > 0);
-                umma_commit(&bar->s_full[st]);
-                umma_commit(&bar->k_empty[st]);
-                return true;
+                umma_commit(&bar->s_full[sb]);
             };
-            // S_0 and S_1 up front; afterwards S_{j+2} is issued right after
-            // PV_j (which consumes P_j from the same TMEM columns; the tensor
-            // pipe executes one thread's MMAs in order), so every K load has
-            // a whole tile of slack and PV_j never waits behind a K load
-            if (ok) ok = issue_qk(0);
-            if (ok && n_tiles > 1) ok = issue_qk(1);
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int st = j & 1;
-                if (!mbar_wait(&bar->p_full[st], (j >> 1) & 1) ||
-                    !mbar_wait(&bar->v_full[st], (j >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // P_j (bf16, 32 columns) overwrote the first half of S_j in TMEM
-                const uint32_t pt = tmem + st * BN;
-                const uint32_t vs = sbase + OFF_V + st * KV_BYTES;
+            // S_0 and S_1 go first; afterwards S_(j+2) is issued right after
+            // P V_j (which consumes P_j from the same TMEM columns; the tensor
+            // pipe executes one thread's MMAs in order)
+            if constexpr (PAGED) {
+                auto issue_qk_ring = [&](int j) -> bool {
+                    const int st = j & 1;
+                    if (!mbar_wait(&bar->kv_full[st], (j >> 1) & 1)) return false;
+                    tc_fence_after();
+                    issue_qk(j, sbase + OFF_KV + st * KV_BYTES);
+                    umma_commit(&bar->kv_empty[st]);
+                    return true;
+                };
+                if (ok) ok = issue_qk_ring(0);
+                if (ok && n_tiles > 1) ok = issue_qk_ring(1);
+                for (int j = 0; j < n_tiles && ok; ++j) {
+                    const int st = j & 1;
+                    if (!mbar_wait(&bar->p_full[st], (j >> 1) & 1) ||
+                        !mbar_wait(&bar->v_full[st], (j >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t pt = tmem + st * BN;
+                    const uint32_t vs = sbase + OFF_KV + (NSTAGE + st) * KV_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_bf16_tmem_a(tmem + COL_O, pt + kk * 8, v_desc(vs, kk), idesc_pv,
-                                     (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bar->o_done);
-                umma_commit(&bar->v_empty[st]);
-                if (j + 2 < n_tiles && !(ok = issue_qk(j + 2))) break;
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        umma_bf16_tmem_a(tmem + COL_O, pt + kk * 8, v_desc(vs, kk), idesc_pv,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&bar->o_done);
+                    umma_commit(&bar->v_empty[st]);
+                    if (j + 2 < n_tiles && !(ok = issue_qk_ring(j + 2))) break;
+                }
+            } else {
+                // S_0 and S_1 from T_0, then S_(j+2) and P V_j from T_(j+1)
+                if (ok) ok = mbar_wait(&bar->kv_full[0], 0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_qk(0, sbase + OFF_KV);
+                    if (n_tiles > 1) issue_qk(1, sbase + OFF_KV + KV_BYTES);
+                    umma_commit(&bar->kv_empty[0]);
+                }
+                for (int j = 0; j < n_tiles && ok; ++j) {
+                    const int sb = j & 1, i = j + 1, st = i & 1;
+                    if (!mbar_wait(&bar->p_full[sb], (j >> 1) & 1) ||
+                        !mbar_wait(&bar->kv_full[st], (i >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // P_j (bf16, 32 columns) overwrote the first half of S_j in TMEM
+                    const uint32_t pt = tmem + sb * BN;
+                    const uint32_t vs = sbase + OFF_KV + st * STAGE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        umma_bf16_tmem_a(tmem + COL_O, pt + kk * 8, v_desc(vs, kk), idesc_pv,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&bar->o_done);
+                    if (j + 2 < n_tiles) issue_qk(j + 2, vs + KV_BYTES);
+                    umma_commit(&bar->kv_empty[st]);
+                }
             }
             if (ok) umma_commit(&bar->all_done); // tracks every MMA issued above
             // and the last o_done arrival lands before the CTA leaves (every
             // MMA is complete once all_done is, so the parity is unambiguous)
             if (ok) ok = mbar_wait(&bar->all_done, 0) && mbar_wait(&bar->o_done, (n_tiles - 1) & 1);
-            // the producer never waits for the last two stage releases: wait
+            // the loaders never wait for the last two stage releases: wait
             // here so that no commit arrives after the CTA has left
-            for (int t = max(0, n_tiles - 2); t < n_tiles && ok; ++t)
-                ok = mbar_wait(&bar->k_empty[t & 1], (t >> 1) & 1) &&
-                     mbar_wait(&bar->v_empty[t & 1], (t >> 1) & 1);
+            if constexpr (PAGED) {
+                for (int t = max(0, n_tiles - 2); t < n_tiles && ok; ++t)
+                    ok = mbar_wait(&bar->kv_empty[t & 1], (t >> 1) & 1) &&
+                         mbar_wait(&bar->v_empty[t & 1], (t >> 1) & 1);
+            } else {
+                for (int t = max(0, n_tiles - 1); t <= n_tiles && ok; ++t)
+                    ok = mbar_wait(&bar->kv_empty[t & 1], (t >> 1) & 1);
+            }
         }
         __syncwarp();
     } else {
