@@ -98,10 +98,22 @@ __device__ __forceinline__ void walk_next(SeqWalk &w, const int32_t *seqlens, in
     }
 }
 
-// CTA whose unit range [c U / P, (c+1) U / P) contains unit u.
-__device__ __forceinline__ int cta_of(long long u, int P, long long U)
+// Work split.  Units are weighed in "cost": unit (hg, b, j) sits at cost
+// position hg * cblk + sc_b + cs + j, where sc_b = (units of sequences
+// 0..b-1) + cs * b, i.e. every sequence carries an overhead of cs
+// unit-equivalents before its first unit (cblk = units + cs * B per head
+// group).  CTA c takes the units whose positions fall in
+// [c Ctot / P, (c+1) Ctot / P).  Starting or ending a sequence costs a CTA a
+// fixed time (q load, partial write, fence, ticket): measured on GB300 as
+// ~3 us, about two units of 64 KB, so a CTA whose range crosses sequence
+// starts gets fewer units and the CTAs finish together (B=64 GQA workload:
+// 102-104 -> 100.4 us).  With cs = 0 this is the plain equal split of units.
+constexpr int kSeqCost = 2;
+
+// CTA whose cost range contains position pos.
+__device__ __forceinline__ int cta_of(long long pos, int P, long long Ctot)
 {
-    return (int)(((u + 1) * P - 1) / U);
+    return (int)(((pos + 1) * P - 1) / Ctot);
 }
 
 template <int D, int BS, int HS>
@@ -121,6 +133,7 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
     __shared__ int s_warp[NW];
     __shared__ int s_total;
     __shared__ long long s_start[2]; // first sequence, its unit offset sb
+    __shared__ long long s_u[2];     // first and one-past-last unit of this CTA
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.batch, mbps = a.max_blocks_per_seq;
@@ -170,25 +183,50 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
     const long long ublk = s_total;
     const long long U = ublk * a.head_groups;
     const int P = gridDim.x;
-    const long long u0 = (long long)blockIdx.x * U / P;
-    const long long u1 = (long long)(blockIdx.x + 1) * U / P;
-    if (u0 < u1) {
-        const long long r0 = u0 % ublk;
-        long long sb = (long long)s_warp[warp] + incl - local;
-        if (r0 >= sb && r0 < sb + local) {
+    // Sequence overhead only when sequences are long against a CTA's share
+    // (the average sequence spans at least half of one), so that most are
+    // split across CTAs and their starts and ends are the expensive kind
+    // (partials, fence, ticket); sequences that fit whole inside a CTA cost
+    // little (workload of 1028 short sequences: 934 us with cs = 0, 946 us
+    // with cs = 2).  Also only when every CTA has several units, so that each
+    // CTA strictly inside a sequence's range still holds units of it.
+    const bool split_heavy = 2 * ublk * P >= (long long)B * U;
+    const int cs = (U >= 4ll * P && split_heavy) ? kSeqCost : 0;
+    const long long cblk = ublk + (long long)cs * B;
+    const long long Ctot = cblk * a.head_groups;
+    {
+        // first unit at or after cost positions c0 and c1
+        const long long sbt = (long long)s_warp[warp] + incl - local; // units before b_lo
+        const long long sct = sbt + (long long)cs * b_lo;             // cost before b_lo
+        const long long span = local + (long long)cs * (b_hi - b_lo);
+        for (int e = 0; e < 2; ++e) {
+            const long long cc = (long long)(blockIdx.x + e) * Ctot / P;
+            if (cc >= Ctot) {
+                if (tid == 0) s_u[e] = U;
+                continue;
+            }
+            const long long r = cc % cblk;
+            if (r < sct || r >= sct + span) continue;
+            long long sb = sbt, sc = sct;
             for (int b = b_lo; b < b_hi; ++b) {
                 bool ok;
-                int n = seq_blocks(__ldg(a.cache_seqlens + b), mbps, BS, &ok);
-                if (r0 < sb + n) {
-                    s_start[0] = b;
-                    s_start[1] = sb;
+                const int n = seq_blocks(__ldg(a.cache_seqlens + b), mbps, BS, &ok);
+                if (r < sc + cs + n) {
+                    const long long j = r < sc + cs ? 0 : r - sc - cs;
+                    s_u[e] = (cc / cblk) * ublk + sb + j;
+                    if (e == 0) {
+                        s_start[0] = b;
+                        s_start[1] = sb;
+                    }
                     break;
                 }
                 sb += n;
+                sc += cs + n;
             }
         }
     }
     __syncthreads();
+    const long long u0 = s_u[0], u1 = s_u[1];
     if (u0 >= u1) return;
 
     SeqWalk w;
@@ -470,8 +508,9 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
                     }
             } else {
                 // partial (acc, m, l) into slot (CTA + segment row)
-                const long long F = (long long)w.hg * ublk + w.sb;
-                const int cfirst = cta_of(F, P, U), clast = cta_of(F + w.nblk - 1, P, U);
+                // cost position of the sequence's first unit
+                const long long F = (long long)w.hg * cblk + w.sb + (long long)cs * w.b + cs;
+                const int cfirst = cta_of(F, P, Ctot), clast = cta_of(F + w.nblk - 1, P, Ctot);
                 const long long segrow = (long long)w.hg * B + w.b;
                 float *slot = a.part + (size_t)(blockIdx.x + segrow) * slot_floats;
                 float *pacc = slot + (size_t)hw * G * D;
@@ -529,7 +568,7 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
                             for (int k = 0; k < DL; ++k) o[g][k] = 0.f;
                         }
                         for (int k = 0; k < nseg; ++k) {
-                            const int c = dense ? cfirst + k : cta_of(F + k, P, U);
+                            const int c = dense ? cfirst + k : cta_of(F + k, P, Ctot);
                             const float *sc = a.part + (size_t)(c + segrow) * slot_floats;
                             const float *ml = sc + (size_t)HS * G * D + ((size_t)hw * G + gb) * 2;
                             const float *pc = sc + ((size_t)hw * G + gb) * D;
