@@ -52,7 +52,7 @@ def source_hash(name: str) -> str:
 # DRAM traffic per launch taken from ncu captures (profiles/), valid only for
 # the kernel source they were measured on.
 NCU_TRAFFIC = {
-    ("pa_decode.cu", "workload2"): {"src": "c7b4ab8baeb88746", "bytes": 560_410_880},
+    ("pa_decode.cu", "workload2"): {"src": "94a367fe8e4dc20a", "bytes": 560_257_792},
     ("pa_varlen_tc.cu", "workload4"): {"src": "4235c5bea6c16267", "bytes": 661_949_440},
 }
 
