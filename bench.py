@@ -44,16 +44,44 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_text(src: str) -> str:
+    """C++/CUDA source with comments and all whitespace removed (string
+    literals kept): two files with equal code text compile to the same
+    kernel, whatever their comments say."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def source_hash(name: str) -> str:
-    with open(os.path.join(ROOT, "paged_kv_cache_300_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel file's code text (comments and layout excluded)."""
+    with open(os.path.join(ROOT, "paged_kv_cache_300_gb300", "csrc", name), encoding="utf-8") as f:
+        return hashlib.sha256(code_text(f.read()).encode()).hexdigest()[:16]
 
 
 # DRAM traffic per launch taken from ncu captures (profiles/), valid only for
-# the kernel source they were measured on.
+# the kernel code they were measured on (source_hash: code text without
+# comments, so a comment edit keeps a capture valid and a code edit does not).
 NCU_TRAFFIC = {
-    ("pa_decode.cu", "workload2"): {"src": "94a367fe8e4dc20a", "bytes": 560_257_792},
-    ("pa_varlen_tc.cu", "workload4"): {"src": "4235c5bea6c16267", "bytes": 661_949_440},
+    ("pa_decode.cu", "workload2"): {"src": "db658851aaf736fb", "bytes": 560_257_792},
+    ("pa_varlen_tc.cu", "workload4"): {"src": "e558d672dcdf96dc", "bytes": 661_949_440},
 }
 
 

@@ -11,10 +11,11 @@
 //  * Stream-K over the flattened work list.  A "unit" is one logical block
 //    of one sequence for one group of HS kv heads; units are ordered (head
 //    group, sequence, logical block) and the persistent grid of P CTAs takes
-//    equal contiguous ranges, so every SM streams the same number of bytes
-//    whatever the length mix.  Every CTA derives the ranges itself from
-//    cache_seqlens (block-wide scan), so the host needs no lengths and no
-//    device-to-host copy.
+//    contiguous ranges of about equal cost (a unit, plus a fixed overhead
+//    per sequence when most sequences are split; see kSeqCost), so every SM
+//    streams about the same number of bytes whatever the length mix.  Every
+//    CTA derives the ranges itself from cache_seqlens (block-wide scan), so
+//    the host needs no lengths and no device-to-host copy.
 //  * A producer warp resolves logical -> physical blocks through the table
 //    (32 entries per coalesced load) and issues TMA tensor loads of the K and
 //    V tiles of each physical block (one 128-byte-swizzled box per kv head

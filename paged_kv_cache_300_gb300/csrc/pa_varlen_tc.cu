@@ -15,8 +15,9 @@
 // over the head groups so the CTAs of one GQA group run side by side.  Tiles
 // are issued from the last (most keys under the causal mask) to the first.
 //
-// Warp roles (192 threads; two CTAs share an SM, 96 KB of shared memory and
-// 256 TMEM columns each, so one CTA's softmax overlaps the other's MMAs):
+// Warp roles (192 threads, 224 for paged keys; two CTAs share an SM, 96 KB
+// of shared memory and 256 TMEM columns each, so one CTA's softmax overlaps
+// the other's MMAs):
 //   warps 0-3  softmax: thread r owns query row r of the tile, which is TMEM
 //              lane r.  It reads its row of S_j from TMEM, masks, keeps the
 //              running max/sum in registers (exp2 domain), writes P_j as bf16
@@ -27,10 +28,12 @@
 //              which the final division by the same running sum cancels
 //              exactly), and in the end divides O by the sum and stores the row.
 //   warp 4     TMA producers: lane 0 loads the Q tile (128 rows) once, then
-//              K tiles of 64 keys (two 64-dim swizzled boxes each); lane 1
-//              loads the V tiles.  Separate 2-stage rings: a K stage frees as
-//              soon as S_j = Q K_j^T is computed, a V stage when O += P_j V_j
-//              is, so K loads run a whole tile ahead.
+//              the K tiles of 64 keys (two 64-dim swizzled boxes each); lane
+//              1 (paged keys: lane 0 of warp 6) loads the V tiles.  Contiguous
+//              keys: one ring whose stage i % 2 holds {V_(i-1), K_(i+1)} as a
+//              single TMA transaction (see NSTAGE below).  Paged keys: a K ring
+//              and a V ring; a K stage frees as soon as S_j = Q K_j^T is
+//              computed, a V stage when O += P_j V_j is.
 //   warp 5     TMEM allocator and MMA issuer (one thread): S_j = Q K_j^T into
 //              one of two TMEM S buffers (M=128, N=64, K=16 per instruction,
 //              both operands K-major from shared memory), then O += P_j V_j
