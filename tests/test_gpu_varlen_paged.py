@@ -126,3 +126,28 @@ def test_mixed_decode_and_prefill_in_one_launch():
     torch.cuda.synchronize()
     assert_close(out_d, mixed[rows.cuda()].double().cpu().numpy(), torch.bfloat16,
                  "decode kernel vs mixed launch")
+
+
+def test_paged_long_request_past_the_staged_table():
+    """bs=8 with 5000 keys: 625 table entries, more than the 512 the loaders
+    stage in shared memory, so the rest are read from the table in global
+    memory."""
+    c = make_varlen(31, [100, 3], [4900, 700], 8, 2, 128, 8)
+    assert c.block_table.shape[1] > 512
+    fused, ref, kf, vf = _both_paths(c)
+    assert torch.equal(fused.view(torch.int16), ref.view(torch.int16))
+    o = oracle.varlen(to_numpy(c.q), bits(kf), bits(vf), c.cu_seq_lens_q.numpy(),
+                      c.cu_seq_lens_k.numpy(), True)
+    assert_close(fused, o, torch.bfloat16, "paged varlen, 5000 keys at bs=8")
+
+
+@pytest.mark.parametrize("heads", [(4, 4), (8, 4), (16, 2)])
+def test_paged_pack_factors(heads):
+    """GQA groups of 1, 2 and 8 query heads through the block table."""
+    hq, hkv = heads
+    c = make_varlen(40 + hq, [3, 200, 65, 1], [40, 100, 0, 8], hq, hkv, 128, 16)
+    fused, ref, kf, vf = _both_paths(c)
+    assert torch.equal(fused.view(torch.int16), ref.view(torch.int16))
+    o = oracle.varlen(to_numpy(c.q), bits(kf), bits(vf), c.cu_seq_lens_q.numpy(),
+                      c.cu_seq_lens_k.numpy(), True)
+    assert_close(fused, o, torch.bfloat16, f"paged varlen, {hq}/{hkv} heads")
