@@ -151,6 +151,19 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
     }
+    {
+        // A small block table is brought into L2 now, each CTA taking a
+        // slice, so that the producer's first table read after the length
+        // scan below hits in L2 instead of waiting on HBM.
+        const size_t tbytes = (size_t)B * mbps * 4;
+        if (tbytes <= ((size_t)4 << 20)) {
+            const size_t lines = (tbytes + 127) / 128;
+            const size_t l0 = lines * blockIdx.x / gridDim.x, l1 = lines * (blockIdx.x + 1) / gridDim.x;
+            const char *tb = reinterpret_cast<const char *>(a.block_table);
+            for (size_t l = l0 + tid; l < l1; l += NT)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(tb + l * 128));
+        }
+    }
 
     // ---- block-wide exclusive scan of the per-sequence block counts
     const int per = (B + NT - 1) / NT;
