@@ -226,26 +226,39 @@ def decode_alg_bytes(case) -> int:
     return case.unique_kv_bytes() + case.io_bytes() + table
 
 
-def run_decode_leg(torch, pa, case, steps, warmup, flush, dist=None, sync_ranks=False):
+def run_decode_leg(torch, pa, case, steps, warmup, flush, dist=None, sync_ranks=False,
+                   contiguous=False):
     """Device time of `steps` pa_decode calls (L2 flushed before each, outside
-    the events).  Returns dict with per-step ms list and wall seconds."""
+    the events).  Returns dict with per-step ms list and wall seconds.
+    `contiguous`: the same logical cache laid out as [B, max_seqlen, Hkv, D]
+    and decoded by the contiguous-cache twin (pa_decode_contiguous)."""
     dev = "cuda"
     t = lambda x: x.to(dev)
-    q, kc, vc, bt, sl, kn, vn = map(t, (case.q, case.k_cache, case.v_cache, case.block_table,
-                                        case.cache_seqlens, case.k_new, case.v_new))
+    q, bt, sl, kn, vn = map(t, (case.q, case.block_table, case.cache_seqlens, case.k_new,
+                                case.v_new))
+    if contiguous:
+        kc, vc = case.contiguous_cache(device=dev)
+        need = pa.pa_decode_contiguous_workspace_size(case.batch, case.num_heads,
+                                                      case.num_kv_heads, case.head_dim)
+    else:
+        kc, vc = t(case.k_cache), t(case.v_cache)
+        need = pa.pa_decode_workspace_size(case.batch, case.num_heads, case.num_kv_heads,
+                                           case.head_dim, case.block_size, case.q.dtype)
     out = torch.empty_like(q)
-    need = pa.pa_decode_workspace_size(case.batch, case.num_heads, case.num_kv_heads,
-                                       case.head_dim, case.block_size, case.q.dtype)
     ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     args = (q, kc, vc, bt, sl, kn, vn, out)
+    if contiguous:
+        step = lambda: pa.pa_decode_contiguous(q, kc, vc, sl, kn, vn, out, workspace=ws,
+                                               dev_err=err)
+    else:
+        step = lambda: pa.pa_decode(*args, workspace=ws, dev_err=err)
     for _ in range(warmup):
-        pa.pa_decode(*args, workspace=ws, dev_err=err)
+        step()
     torch.cuda.synchronize()
     # one decode step captured as a CUDA graph: the timed loop replays it, so
     # the per-step host work (argument checks, descriptor encoding) is paid
     # once, as a serving loop would
-    step = lambda: pa.pa_decode(*args, workspace=ws, dev_err=err)
     graph = None
     try:
         g = torch.cuda.CUDAGraph()
@@ -308,19 +321,24 @@ def run_decode_e2e(torch, pa, case, res, steps, flush):
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in srcs)
     d2h = hout.numel() * hout.element_size()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     torch.cuda.synchronize()
-    for e0, e1 in evs:
+    for e in evs:
         flush.zero_()
-        e0.record()
+        e[0].record()
         dbuf.copy_(hbuf, non_blocking=True)
+        e[1].record()
         pa.pa_decode(dq, kc, vc, dbt, dsl, dkn, dvn, out, workspace=ws, dev_err=err)
+        e[2].record()
         hout.copy_(out, non_blocking=True)
-        e1.record()
+        e[3].record()
     torch.cuda.synchronize()
-    ms = [a.elapsed_time(b) for a, b in evs]
-    return sum(ms) / len(ms), h2d, d2h
+    n = len(evs)
+    ms = sum(e[0].elapsed_time(e[3]) for e in evs) / n
+    parts = {"h2d_ms": round(sum(e[0].elapsed_time(e[1]) for e in evs) / n, 5),
+             "call_ms": round(sum(e[1].elapsed_time(e[2]) for e in evs) / n, 5),
+             "d2h_ms": round(sum(e[2].elapsed_time(e[3]) for e in evs) / n, 5)}
+    return ms, h2d, d2h, parts
 
 
 # --------------------------------------------------------------------------
@@ -529,7 +547,8 @@ def main(argv=None):
     value = ub_all / ms / 1e6
     main = leg_summary(case, res["ms"], peaks)
     main_launch = res["launch"]
-    e2e_ms, h2d, d2h = run_decode_e2e(torch, pa, case, res, max(10, args.steps // 2), flush)
+    e2e_ms, h2d, d2h, e2e_parts = run_decode_e2e(torch, pa, case, res, max(10, args.steps // 2),
+                                                  flush)
     e2e_ms = dist.max(torch, e2e_ms)
     del res
     torch.cuda.empty_cache()
@@ -542,18 +561,36 @@ def main(argv=None):
             extra[key] = leg_summary(c, r["ms"], peaks)
             del r, c
             torch.cuda.empty_cache()
-        # paging overhead: the main workload again with every sequence's blocks
-        # adjacent in the pool (the layout of a non-paged cache), same kernel
+        # paging overhead, two ways.  (1) Placement: the main workload again
+        # with every sequence's blocks adjacent in the pool, same kernel.
+        # (2) The contiguous-cache twin: the same logical cache laid out as
+        # [B, max_seqlen, Hkv, D] and decoded by pa_decode_contiguous (no
+        # block table), against pa_decode on the paged pool.
         c = decode_config(2, seed_offset=dist.rank, contiguous=True)
         r = run_decode_leg(torch, pa, c, min(args.steps, 20), args.warmup, flush)
         cms = sum(r["ms"]) / len(r["ms"])
-        extra["paging_overhead"] = {
+        overhead = {"placement": {
             "workload": c.name,
-            "contiguous_ms": round(cms, 5), "scattered_ms": round(ms, 5),
-            "scattered_over_contiguous": round(ms / cms, 4),
-            "note": "same kernel and data; only the physical placement of the blocks differs"}
+            "adjacent_blocks_ms": round(cms, 5), "scattered_blocks_ms": round(ms, 5),
+            "scattered_over_adjacent": round(ms / cms, 4),
+            "note": "same paged kernel and data; only the physical placement of the blocks "
+                    "differs"}}
         del r, c
         torch.cuda.empty_cache()
+        for idx, paged_ms in ((2, ms), (3, extra["decode_long_context"]["ms"])):
+            c = decode_config(idx, seed_offset=dist.rank if idx == 2 else 0)
+            r = run_decode_leg(torch, pa, c, min(args.steps, 20), args.warmup, flush,
+                               contiguous=True)
+            cms = sum(r["ms"]) / len(r["ms"])
+            overhead[f"paged_over_contiguous_workload{idx}"] = {
+                "workload": c.name, "paged_ms": round(paged_ms, 5),
+                "contiguous_ms": round(cms, 5), "paged_over_contiguous": round(paged_ms / cms, 4),
+                "contiguous_kv_GBps": round(c.unique_kv_bytes() / cms / 1e6, 1),
+                "note": "pa_decode (block table, scattered blocks) vs pa_decode_contiguous "
+                        "(the same kernel code over a [B, max_seqlen, Hkv, D] cache, no table)"}
+            del r, c
+            torch.cuda.empty_cache()
+        extra["paging_overhead"] = overhead
         vc = varlen_config(4)
         try:
             upd_ms, att_ms, scat_ms, patt_ms = run_varlen_leg(torch, pa, vc, min(args.steps, 20),
@@ -606,7 +643,7 @@ def main(argv=None):
                          peak_source=f"{peak_kind} hbm_gbs (copy)"),
         "e2e": {"value": round(ub_all / e2e_ms / 1e6, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 5)},
+                "ms_per_step": round(e2e_ms, 5), **e2e_parts},
         "gpu_launches": args.steps,
         "clocks": clk,
     }

@@ -52,7 +52,9 @@
  *    *dev_err when it wants to.
  *
  * Supported: dtype PA_BF16 or PA_F32; head_dim 64 or 128; for PA_BF16
- * decode, block_size 16 or 32 and num_heads / num_kv_heads <= 8.
+ * decode, block_size 16 or 32 and num_heads / num_kv_heads <= 8.  The bf16
+ * varlen calls (pa_varlen, pa_varlen_paged) run the tensor-core kernel, built
+ * for head_dim 128 only: head_dim 64 returns PA_ERR_UNSUPPORTED there.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -156,6 +158,37 @@ int pa_decode_static_scratch(const void *q, void *k_cache, void *v_cache,
                              int32_t *dev_err, void *stream);
 
 /*
+ * The contiguous-cache twin of pa_decode, for measuring what paging costs:
+ * "39 · PagedAttention" (inference-notes), sections "Ghi chú" and
+ * "4. Có miễn phí không?", compares a paged attention kernel with one over a
+ * contiguous cache.  This call is that contiguous kernel: the same decode
+ * kernel with the block table taken out.
+ *
+ * k_cache, v_cache  [batch, max_seqlen, num_kv_heads, head_dim]: sequence b
+ *                   holds its position t at [b, t].  Nothing is shared
+ *                   between sequences and no table is read.
+ * For every sequence b, with L = cache_seqlens[b] (read only):
+ *  1. append: k_new[b], v_new[b] are copied bit for bit to [b, L];
+ *  2. attend: out[b, h] = softmax(q[b, h] . K_j * scale) V_j over positions
+ *     j = 0..L of row b.
+ * L + 1 > max_seqlen (or L < 0) sets PA_DEVERR_OVERFLOW and zeroes the
+ * sequence's output.  Positions past L of a row are never used in the
+ * result (whatever they hold).  bf16 only (dtype PA_BF16 implied); head_dim
+ * 64 or 128; num_heads / num_kv_heads <= 8; batch * max_seqlen < 2^31.
+ * workspace: as pa_decode, at least pa_decode_contiguous_workspace_size(...)
+ * bytes, zero-filled before first use.  For the same logical cache contents,
+ * the result equals pa_decode's with block_size 16 (head_dim 128) or 32
+ * (head_dim 64) bit for bit.
+ */
+size_t pa_decode_contiguous_workspace_size(int batch, int num_heads, int num_kv_heads,
+                                           int head_dim);
+int pa_decode_contiguous(const void *q, void *k_cache, void *v_cache,
+                         const int32_t *cache_seqlens, const void *k_new, const void *v_new,
+                         void *out, int batch, int num_heads, int num_kv_heads, int head_dim,
+                         int max_seqlen, float softmax_scale, void *workspace,
+                         size_t workspace_bytes, int32_t *dev_err, void *stream);
+
+/*
  * Varlen cache update ("Jalur Varlen" -> "Perilaku cache").
  *
  * k_chunk, v_chunk [total_q, num_kv_heads, head_dim]: the new tokens of all
@@ -185,7 +218,9 @@ int pa_cache_update(const void *k_chunk, const void *v_chunk, const int32_t *cu_
  * largest q / k length (they size the launch).  causal != 0 masks
  * bottom-right: query i of a request with lengths (ql, kl) sees key j iff
  * j <= i + kl - ql.  A query that sees no key gets a zero output row.
- * PA_BF16 runs on the tcgen05 tensor cores; PA_F32 on CUDA cores.
+ * PA_BF16 runs on the tcgen05 tensor cores and needs head_dim 128
+ * (head_dim 64 returns PA_ERR_UNSUPPORTED); PA_F32 runs on CUDA cores with
+ * head_dim 64 or 128.
  */
 int pa_varlen(const void *q, const void *k, const void *v, const int32_t *cu_seq_lens_q,
               const int32_t *cu_seq_lens_k, int max_length_q, int max_length_k, int causal,

@@ -8,6 +8,8 @@ built, or no GPU is present, calls raise.
 
     pa_decode        decode step: in-place append + attention, one query per
                      sequence, through block_table
+    pa_decode_contiguous  the same step over a contiguous cache (no table):
+                     the twin that measures what paging costs
     pa_cache_update  scatter a packed varlen chunk into the paged pool
                      (optionally gather prefix + chunk into packed k/v)
     pa_varlen        packed variable-length attention (bf16: tcgen05)
@@ -23,6 +25,7 @@ import torch
 
 __all__ = [
     "PAError", "library_path", "load", "pa_decode", "pa_decode_static_scratch",
+    "pa_decode_contiguous", "pa_decode_contiguous_workspace_size",
     "pa_cache_update", "pa_varlen", "pa_varlen_paged",
     "pa_decode_workspace_size", "pa_status_string", "pa_version", "DEVERR_BAD_BLOCK",
     "DEVERR_OVERFLOW", "DEVERR_BAD_CU", "DEVERR_TIMEOUT",
@@ -67,6 +70,10 @@ def load():
         lib.pa_decode.restype = i
         lib.pa_decode_static_scratch.argtypes = [p] * 8 + [i] * 7 + [f, p, p]
         lib.pa_decode_static_scratch.restype = i
+        lib.pa_decode_contiguous_workspace_size.argtypes = [i] * 4
+        lib.pa_decode_contiguous_workspace_size.restype = sz
+        lib.pa_decode_contiguous.argtypes = [p] * 7 + [i] * 5 + [f, p, sz, p, p]
+        lib.pa_decode_contiguous.restype = i
         lib.pa_cache_update.argtypes = [p] * 10 + [i] * 8 + [i, p, p]
         lib.pa_cache_update.restype = i
         lib.pa_varlen.argtypes = [p] * 5 + [i] * 3 + [p] + [i] * 6 + [i, f, p, p]
@@ -176,9 +183,8 @@ def pa_decode(q, k_cache, v_cache, block_table, cache_seqlens, k_new, v_new, out
     elif out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("out must match q")
     lib = load()
-    need = int(lib.pa_decode_workspace_size(b, hq, hkv, d, bs, dt))
     if workspace is None:
-        workspace = _workspace(dev, need)
+        workspace = _workspace(dev, int(lib.pa_decode_workspace_size(b, hq, hkv, d, bs, dt)))
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                        _ptr(cache_seqlens), _ptr(k_new), _ptr(v_new), _ptr(out), b, hq, hkv, d,
@@ -208,6 +214,46 @@ def pa_decode_static_scratch(q, k_cache, v_cache, block_table, cache_seqlens, k_
                                          b, hq, hkv, d, nb, bs, block_table.shape[1],
                                          float(softmax_scale), _ptr(dev_err), _stream(stream))
     _call("pa_decode_static_scratch", rc)
+    return out
+
+
+def pa_decode_contiguous_workspace_size(batch, num_heads, num_kv_heads, head_dim) -> int:
+    return int(load().pa_decode_contiguous_workspace_size(batch, num_heads, num_kv_heads,
+                                                          head_dim))
+
+
+def pa_decode_contiguous(q, k_cache, v_cache, cache_seqlens, k_new, v_new, out=None,
+                         softmax_scale: float = 0.0, workspace=None, dev_err=None, stream=None):
+    """Decode step over a contiguous cache (see include/pa.h): q [B, Hq, D];
+    k_cache/v_cache [B, max_seqlen, Hkv, D] (the new token is written in
+    place at [b, cache_seqlens[b]]); k_new/v_new [B, Hkv, D].  bf16 only.
+    Returns out [B, Hq, D]."""
+    dev = _check_dev(q, k_cache, v_cache, cache_seqlens, k_new, v_new, out, workspace, dev_err)
+    _i32(cache_seqlens, "cache_seqlens")
+    _i32(dev_err, "dev_err")
+    if q.dtype != torch.bfloat16:
+        raise TypeError("pa_decode_contiguous takes bfloat16 tensors")
+    for t in (k_cache, v_cache, k_new, v_new):
+        if t.dtype != q.dtype:
+            raise TypeError("q, k_cache, v_cache, k_new, v_new must share a dtype")
+    b, hq, d = q.shape
+    b2, lmax, hkv, d2 = k_cache.shape
+    if b2 != b or d2 != d or v_cache.shape != k_cache.shape or k_new.shape != (b, hkv, d) or \
+            v_new.shape != (b, hkv, d) or cache_seqlens.shape != (b,):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    lib = load()
+    if workspace is None:
+        workspace = _workspace(dev, int(lib.pa_decode_contiguous_workspace_size(b, hq, hkv, d)))
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.pa_decode_contiguous(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens),
+                                  _ptr(k_new), _ptr(v_new), _ptr(out), b, hq, hkv, d, lmax,
+                                  float(softmax_scale), _ptr(workspace), wbytes, _ptr(dev_err),
+                                  _stream(stream))
+    _call("pa_decode_contiguous", rc)
     return out
 
 

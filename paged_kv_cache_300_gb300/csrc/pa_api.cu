@@ -55,6 +55,73 @@ int encode_rows_map(CUtensorMap *map, const void *base, uint64_t rows, int heads
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_LAUNCH;
 }
 
+// 3-D bf16 view of a row-major [rows, heads, head_dim] tensor as
+// (64 dims, rows, heads * head_dim / 64 halves): dimension 1 (rows) has the
+// row stride and dimension 2 steps 128 bytes.  One box is box_rows rows of
+// the box_heads heads starting at a given half, and lands in shared memory
+// as box_heads * head_dim / 64 slabs of box_rows 128-byte rows, slab after
+// slab, 128-byte swizzled.
+int encode_unit_map(CUtensorMap *map, const void *base, uint64_t rows, int heads, int head_dim,
+                    int box_rows, int box_heads)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr) return PA_ERR_DEVICE;
+    const cuuint64_t dims[3] = {64, rows, (cuuint64_t)heads * head_dim / 64};
+    const cuuint64_t strides[2] = {(cuuint64_t)heads * head_dim * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)(box_heads * head_dim / 64)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_LAUNCH;
+}
+
+// Encoded tensor maps of recent calls, keyed on everything the encoding
+// reads (base address, view, sizes, box): a map depends on nothing else, so
+// a hit is the same 128 bytes the encoder would write.  Repeated calls on the
+// same cache (every step of a serving loop) then skip the encoder.
+struct MapKey {
+    const void *base;
+    uint64_t rows;
+    int heads, head_dim, box_rows, box_heads, kind;
+    bool operator==(const MapKey &o) const
+    {
+        return base == o.base && rows == o.rows && heads == o.heads && head_dim == o.head_dim &&
+               box_rows == o.box_rows && box_heads == o.box_heads && kind == o.kind;
+    }
+};
+constexpr int kMapCacheSize = 32;
+static std::mutex g_map_mu;
+static MapKey g_map_keys[kMapCacheSize];
+static CUtensorMap g_maps[kMapCacheSize];
+static int g_map_used = 0, g_map_next = 0;
+
+// kind 0: encode_rows_map, 1: encode_unit_map, 2: encode_packed_q_map (head_dim
+// then carries the pack factor, box_rows the queries per box)
+static int cached_map(CUtensorMap *map, int kind, const void *base, uint64_t rows, int heads,
+                      int head_dim, int box_rows, int box_heads)
+{
+    const MapKey key{base, rows, heads, head_dim, box_rows, box_heads, kind};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        for (int i = 0; i < g_map_used; ++i)
+            if (g_map_keys[i] == key) {
+                *map = g_maps[i];
+                return PA_OK;
+            }
+    }
+    const int rc = kind == 0   ? encode_rows_map(map, base, rows, heads, head_dim, box_rows)
+                   : kind == 1 ? encode_unit_map(map, base, rows, heads, head_dim, box_rows, box_heads)
+                               : encode_packed_q_map(map, base, rows, heads, head_dim, box_rows);
+    if (rc != PA_OK) return rc;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    const int i = g_map_used < kMapCacheSize ? g_map_used++ : g_map_next;
+    g_map_next = (i + 1) % kMapCacheSize;
+    g_map_keys[i] = key;
+    g_maps[i] = *map;
+    return PA_OK;
+}
+
 // 4-D bf16 view of q [rows, heads, 128] as (64 dims, 2 halves, heads, rows);
 // one box is one 64-dim half of `pack` consecutive heads for `box_queries`
 // consecutive rows, landing in shared memory as box_queries * pack rows of
@@ -85,6 +152,16 @@ int varlen_pack_factor(int num_heads, int num_kv_heads)
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int decode_check_pointers(const void *q, const void *k_cache, const void *v_cache,
+                          const void *k_new, const void *v_new, const void *out)
+{
+    if (!q || !k_cache || !v_cache || !k_new || !v_new || !out) return PA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) ||
+        !aligned16(v_new) || !aligned16(out))
+        return PA_ERR_SHAPE;
+    return PA_OK;
+}
 
 }  // namespace pa
 
@@ -131,11 +208,9 @@ int pa_decode(const void *q, void *k_cache, void *v_cache, const int32_t *block_
         return PA_ERR_SHAPE;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (batch == 0) return PA_OK;
-    if (!q || !k_cache || !v_cache || !block_table || !cache_seqlens || !k_new || !v_new || !out)
-        return PA_ERR_NULL;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) ||
-        !aligned16(v_new) || !aligned16(out))
-        return PA_ERR_SHAPE;
+    if (!block_table || !cache_seqlens) return PA_ERR_NULL;
+    int rc = decode_check_pointers(q, k_cache, v_cache, k_new, v_new, out);
+    if (rc != PA_OK) return rc;
     if ((long long)num_blocks * block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -161,7 +236,7 @@ int pa_decode(const void *q, void *k_cache, void *v_cache, const int32_t *block_
     if (dtype == PA_F32) return decode_f32_launch(a, head_dim, block_size, s);
 
     DecodePlan plan;
-    int rc = decode_bf16_plan(batch, num_heads, num_kv_heads, head_dim, block_size, &plan);
+    rc = decode_bf16_plan(batch, num_heads, num_kv_heads, head_dim, block_size, &plan);
     if (rc != PA_OK) return rc;
     if (workspace == nullptr || workspace_bytes < decode_workspace_bytes(plan) ||
         !aligned16(workspace))
@@ -172,11 +247,76 @@ int pa_decode(const void *q, void *k_cache, void *v_cache, const int32_t *block_
     a.nstages = plan.nstages;
     CUtensorMap tm_k, tm_v;
     const uint64_t rows = (uint64_t)num_blocks * block_size;
-    if ((rc = encode_rows_map(&tm_k, k_cache, rows, num_kv_heads, head_dim, block_size)) != PA_OK)
+    const int hs = plan.heads_per_cta;
+    if ((rc = cached_map(&tm_k, 1, k_cache, rows, num_kv_heads, head_dim, block_size, hs)) != PA_OK)
         return rc;
-    if ((rc = encode_rows_map(&tm_v, v_cache, rows, num_kv_heads, head_dim, block_size)) != PA_OK)
+    if ((rc = cached_map(&tm_v, 1, v_cache, rows, num_kv_heads, head_dim, block_size, hs)) != PA_OK)
         return rc;
     return decode_bf16_launch(a, head_dim, block_size, plan, tm_k, tm_v, s);
+}
+
+size_t pa_decode_contiguous_workspace_size(int batch, int num_heads, int num_kv_heads,
+                                           int head_dim)
+{
+    if (batch <= 0 || (head_dim != 64 && head_dim != 128)) return 0;
+    DecodePlan plan;
+    if (decode_bf16_plan(batch, num_heads, num_kv_heads, head_dim, contig_unit(head_dim), &plan,
+                         true) != PA_OK)
+        return 0;
+    return decode_workspace_bytes(plan);
+}
+
+int pa_decode_contiguous(const void *q, void *k_cache, void *v_cache,
+                         const int32_t *cache_seqlens, const void *k_new, const void *v_new,
+                         void *out, int batch, int num_heads, int num_kv_heads, int head_dim,
+                         int max_seqlen, float softmax_scale, void *workspace,
+                         size_t workspace_bytes, int32_t *dev_err, void *stream)
+{
+    if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seqlen <= 0 ||
+        num_heads % num_kv_heads != 0)
+        return PA_ERR_SHAPE;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (batch == 0) return PA_OK;
+    if (!cache_seqlens) return PA_ERR_NULL;
+    int rc = decode_check_pointers(q, k_cache, v_cache, k_new, v_new, out);
+    if (rc != PA_OK) return rc;
+    if ((long long)batch * max_seqlen >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    const int unit = contig_unit(head_dim);
+    DecodePlan plan;
+    rc = decode_bf16_plan(batch, num_heads, num_kv_heads, head_dim, unit, &plan, true);
+    if (rc != PA_OK) return rc;
+    if (workspace == nullptr || workspace_bytes < decode_workspace_bytes(plan) ||
+        !aligned16(workspace))
+        return PA_ERR_WORKSPACE;
+    DecodeArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.cache_seqlens = cache_seqlens;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.out = out;
+    a.dev_err = dev_err;
+    a.batch = batch;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.max_seqlen = max_seqlen;
+    a.group = num_heads / num_kv_heads;
+    a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
+    a.scale_log2 = a.scale * 1.4426950408889634f;
+    a.tickets = static_cast<int32_t *>(workspace);
+    a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kTicketRegionBytes);
+    a.head_groups = plan.head_groups;
+    a.nstages = plan.nstages;
+    CUtensorMap tm_k, tm_v;
+    const uint64_t rows = (uint64_t)batch * max_seqlen;
+    const int hs = plan.heads_per_cta;
+    if ((rc = cached_map(&tm_k, 1, k_cache, rows, num_kv_heads, head_dim, unit, hs)) != PA_OK)
+        return rc;
+    if ((rc = cached_map(&tm_v, 1, v_cache, rows, num_kv_heads, head_dim, unit, hs)) != PA_OK)
+        return rc;
+    return decode_bf16_launch(a, head_dim, unit, plan, tm_k, tm_v, static_cast<cudaStream_t>(stream),
+                              true);
 }
 
 int pa_cache_update(const void *k_chunk, const void *v_chunk, const int32_t *cu_seq_lens_q,
@@ -264,15 +404,15 @@ int pa_varlen(const void *q, const void *k, const void *v, const int32_t *cu_seq
     CUtensorMap tm_q, tm_k, tm_v;
     int rc;
     a.pack = varlen_pack_factor(num_heads, num_kv_heads);
-    if ((rc = encode_packed_q_map(&tm_q, q, (uint64_t)total_q, num_heads, a.pack,
-                                  kVarlenQRows / a.pack)) != PA_OK)
+    if ((rc = cached_map(&tm_q, 2, q, (uint64_t)total_q, num_heads, a.pack, kVarlenQRows / a.pack,
+                         0)) != PA_OK)
         return rc;
     if (total_k > 0) {
-        if ((rc = encode_rows_map(&tm_k, k, (uint64_t)total_k, num_kv_heads, head_dim,
-                                 kVarlenKRows)) != PA_OK)
+        if ((rc = cached_map(&tm_k, 0, k, (uint64_t)total_k, num_kv_heads, head_dim,
+                             kVarlenKRows, 0)) != PA_OK)
             return rc;
-        if ((rc = encode_rows_map(&tm_v, v, (uint64_t)total_k, num_kv_heads, head_dim,
-                                 kVarlenKRows)) != PA_OK)
+        if ((rc = cached_map(&tm_v, 0, v, (uint64_t)total_k, num_kv_heads, head_dim,
+                             kVarlenKRows, 0)) != PA_OK)
             return rc;
     } else {
         tm_k = tm_q;
@@ -325,12 +465,12 @@ int pa_varlen_paged(const void *q, const void *k_cache, const void *v_cache,
     int rc;
     const uint64_t rows = (uint64_t)num_blocks * block_size;
     a.pack = varlen_pack_factor(num_heads, num_kv_heads);
-    if ((rc = encode_packed_q_map(&tm_q, q, (uint64_t)total_q, num_heads, a.pack,
-                                  kVarlenQRows / a.pack)) != PA_OK)
+    if ((rc = cached_map(&tm_q, 2, q, (uint64_t)total_q, num_heads, a.pack, kVarlenQRows / a.pack,
+                         0)) != PA_OK)
         return rc;
-    if ((rc = encode_rows_map(&tm_k, k_cache, rows, num_kv_heads, head_dim, block_size)) != PA_OK)
+    if ((rc = cached_map(&tm_k, 0, k_cache, rows, num_kv_heads, head_dim, block_size, 0)) != PA_OK)
         return rc;
-    if ((rc = encode_rows_map(&tm_v, v_cache, rows, num_kv_heads, head_dim, block_size)) != PA_OK)
+    if ((rc = cached_map(&tm_v, 0, v_cache, rows, num_kv_heads, head_dim, block_size, 0)) != PA_OK)
         return rc;
     return varlen_paged_bf16_launch(a, tm_q, tm_k, tm_v, static_cast<cudaStream_t>(stream));
 }

@@ -70,21 +70,24 @@ struct SeqWalk {
     long long sb; // units of sequences 0..b-1 within the head group
 };
 
-__device__ __forceinline__ int seq_blocks(int L, int mbps, int bs, bool *ok)
+// Blocks of a sequence with L cached tokens once the new token is appended;
+// `cap` is the positions a sequence can hold (the table's blocks times the
+// block size, or the rows of a contiguous cache).
+__device__ __forceinline__ int seq_blocks(int L, long long cap, int bs, bool *ok)
 {
-    *ok = L >= 0 && (long long)L + 1 <= (long long)mbps * bs;
+    *ok = L >= 0 && (long long)L + 1 <= cap;
     return *ok ? (L + bs) / bs : 1;
 }
 
-__device__ __forceinline__ void walk_load(SeqWalk &w, const int32_t *seqlens, int mbps, int bs)
+__device__ __forceinline__ void walk_load(SeqWalk &w, const int32_t *seqlens, long long cap, int bs)
 {
     bool ok;
     int L = __ldg(seqlens + w.b);
-    w.nblk = seq_blocks(L, mbps, bs, &ok);
+    w.nblk = seq_blocks(L, cap, bs, &ok);
     w.len = ok ? L : -1;
 }
 
-__device__ __forceinline__ void walk_next(SeqWalk &w, const int32_t *seqlens, int mbps, int bs,
+__device__ __forceinline__ void walk_next(SeqWalk &w, const int32_t *seqlens, long long cap, int bs,
                                           int batch)
 {
     if (++w.j == w.nblk) {
@@ -95,7 +98,7 @@ __device__ __forceinline__ void walk_next(SeqWalk &w, const int32_t *seqlens, in
             w.sb = 0;
             ++w.hg;
         }
-        walk_load(w, seqlens, mbps, bs);
+        walk_load(w, seqlens, cap, bs);
     }
 }
 
@@ -117,7 +120,13 @@ __device__ __forceinline__ int cta_of(long long pos, int P, long long Ctot)
     return (int)(((pos + 1) * P - 1) / Ctot);
 }
 
-template <int D, int BS, int HS>
+// CONTIG = false: the paged cache [num_blocks, BS, Hkv, D] through the block
+// table.  CONTIG = true: the contiguous-cache twin, a cache [batch,
+// max_seqlen, Hkv, D] whose sequence b holds position t at row
+// b * max_seqlen + t; it has no table, and a unit is BS consecutive rows.
+// Everything after the address of a unit's rows is the same code, so for the
+// same logical cache and the same split both give the same bits.
+template <int D, int BS, int HS, bool CONTIG>
 __global__ void __launch_bounds__((HS + 1) * 32, 1)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a)
@@ -138,6 +147,7 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.batch, mbps = a.max_blocks_per_seq;
+    const long long cap = CONTIG ? (long long)a.max_seqlen : (long long)mbps * BS;
     const __nv_bfloat16 *qp = static_cast<const __nv_bfloat16 *>(a.q);
 
     if (tid == 0) {
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
     }
-    {
+    if constexpr (!CONTIG) {
         // A small block table is brought into L2 now, each CTA taking a
         // slice, so that the producer's first table read after the length
         // scan below hits in L2 instead of waiting on HBM.
@@ -171,7 +181,7 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
     int local = 0;
     for (int b = b_lo; b < b_hi; ++b) {
         bool ok;
-        local += seq_blocks(__ldg(a.cache_seqlens + b), mbps, BS, &ok);
+        local += seq_blocks(__ldg(a.cache_seqlens + b), cap, BS, &ok);
         if (!ok && blockIdx.x == 0) flag_error(a.dev_err, PA_DEVERR_OVERFLOW);
     }
     int incl = local;
@@ -224,7 +234,7 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
             long long sb = sbt, sc = sct;
             for (int b = b_lo; b < b_hi; ++b) {
                 bool ok;
-                const int n = seq_blocks(__ldg(a.cache_seqlens + b), mbps, BS, &ok);
+                const int n = seq_blocks(__ldg(a.cache_seqlens + b), cap, BS, &ok);
                 if (r < sc + cs + n) {
                     const long long j = r < sc + cs ? 0 : r - sc - cs;
                     s_u[e] = (cc / cblk) * ublk + sb + j;
@@ -247,53 +257,60 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
     w.hg = (int)(u0 / ublk);
     w.b = (int)s_start[0];
     w.sb = s_start[1];
-    walk_load(w, a.cache_seqlens, mbps, BS);
+    walk_load(w, a.cache_seqlens, cap, BS);
     w.j = (int)(u0 % ublk - w.sb);
 
     if (warp == HS) {
-        // ================= producer: block table -> TMA =================
+        // ================= producer: unit rows -> TMA =================
+        // One box per unit for K and one for V: the cache is viewed as
+        // (64 dims, rows, kv-head halves), so a box of BS rows x the HS*KB
+        // halves of this head group lands as HS*KB slabs of BS 128-byte rows,
+        // slab (head, half) at (head * KB + half) * BOX_BYTES: the layout the
+        // consumers read, with the 128-byte swizzle phase = row % 8.
         int tab_b = -1, tab_hg = -1, tab_j0 = 0, tab_entry = -1;
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
         for (long long u = u0; u < u1; ++u) {
-            if (w.b != tab_b || w.hg != tab_hg || w.j >= tab_j0 + 32) {
-                tab_b = w.b;
-                tab_hg = w.hg;
-                tab_j0 = w.j;
-                const int jj = w.j + lane;
-                tab_entry = (w.len >= 0 && jj < w.nblk)
-                                ? __ldg(a.block_table + (size_t)w.b * mbps + jj)
-                                : -1;
+            int row0 = -1; // cache row of the unit's first token, -1: nothing to load
+            if constexpr (CONTIG) {
+                if (w.len >= 0) row0 = w.b * a.max_seqlen + w.j * BS;
+            } else {
+                if (w.b != tab_b || w.hg != tab_hg || w.j >= tab_j0 + 32) {
+                    tab_b = w.b;
+                    tab_hg = w.hg;
+                    tab_j0 = w.j;
+                    const int jj = w.j + lane;
+                    tab_entry = (w.len >= 0 && jj < w.nblk)
+                                    ? __ldg(a.block_table + (size_t)w.b * mbps + jj)
+                                    : -1;
+                }
+                const int p = __shfl_sync(kFull, tab_entry, w.j - tab_j0);
+                const bool valid = w.len >= 0 && p >= 0 && p < a.num_blocks;
+                if (w.len >= 0 && !valid && lane == 0) flag_error(a.dev_err, PA_DEVERR_BAD_BLOCK);
+                row0 = valid ? p * BS : -1;
             }
-            const int p = __shfl_sync(kFull, tab_entry, w.j - tab_j0);
-            const bool valid = w.len >= 0 && p >= 0 && p < a.num_blocks;
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                if (w.len >= 0 && !valid) flag_error(a.dev_err, PA_DEVERR_BAD_BLOCK);
-                stage_phys[stage] = valid ? p : -1;
-                if (valid)
+                stage_phys[stage] = row0;
+                if (row0 >= 0)
                     mbar_arrive_expect_tx(&full[stage], Gm::STAGE_BYTES);
                 else
                     mbar_arrive(&full[stage]);
             }
             __syncwarp();
-            if (valid && lane < 2 * HS * Gm::KB) {
-                const int kv = lane / (HS * Gm::KB), rem = lane % (HS * Gm::KB);
-                const int hw = rem / Gm::KB, kb = rem % Gm::KB;
-                const uint32_t dst = smem_u32(smem + stage * Gm::STAGE_BYTES + kv * Gm::KV_BYTES +
-                                              (hw * Gm::KB + kb) * Gm::BOX_BYTES);
-                tma_load_3d(dst, kv ? &tm_v : &tm_k, &full[stage], 0,
-                            (w.hg * HS + hw) * Gm::KB + kb, p * BS);
+            if (row0 >= 0 && lane < 2) {
+                const uint32_t dst = smem_u32(smem + stage * Gm::STAGE_BYTES + lane * Gm::KV_BYTES);
+                tma_load_3d(dst, lane ? &tm_v : &tm_k, &full[stage], 0, row0, w.hg * HS * Gm::KB);
             }
             if (++stage == nst) {
                 stage = 0;
                 phase ^= 1;
             }
-            walk_next(w, a.cache_seqlens, mbps, BS, B);
+            walk_next(w, a.cache_seqlens, cap, BS, B);
         }
         if (!ok && lane == 0) flag_error(a.dev_err, PA_DEVERR_TIMEOUT);
         return;
@@ -365,7 +382,7 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
             if (lane == 0) flag_error(a.dev_err, PA_DEVERR_TIMEOUT);
             return;
         }
-        const int p = stage_phys[stage];
+        const int p = stage_phys[stage]; // first cache row of the unit, or -1
         const int L = w.len;
         bad |= (p < 0);
         uint8_t *kst = smem + stage * Gm::STAGE_BYTES + hw * Gm::HEAD_BYTES;
@@ -376,7 +393,7 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
             constexpr int EPL = D / 32;
             const int slot = L % BS, d0 = lane * EPL;
             const size_t src = ((size_t)w.b * Hkv + kvh) * D + d0;
-            const size_t dst = (((size_t)p * BS + slot) * Hkv + kvh) * D + d0;
+            const size_t dst = ((size_t)(p + slot) * Hkv + kvh) * D + d0;
             const uint32_t so = (d0 >> 6) * Gm::BOX_BYTES + sw128_offset(slot, d0 & 63);
             const __nv_bfloat16 *kn = static_cast<const __nv_bfloat16 *>(a.k_new);
             const __nv_bfloat16 *vn = static_cast<const __nv_bfloat16 *>(a.v_new);
@@ -629,7 +646,7 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
             }
             open = false;
         }
-        walk_next(w, a.cache_seqlens, mbps, BS, B);
+        walk_next(w, a.cache_seqlens, cap, BS, B);
     }
 }
 
@@ -715,13 +732,13 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const DecodeArgs a, int
     for (int k = 0; k < EPL; ++k) out[k] = acc[k] * inv;
 }
 
-template <int D, int BS, int HS>
+template <int D, int BS, int HS, bool CONTIG>
 int launch_bf16(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &tm_k,
                 const CUtensorMap &tm_v, cudaStream_t s)
 {
     // the shared-memory attribute was set when the plan was made
-    decode_bf16_kernel<D, BS, HS><<<plan.ctas, Geom<D, BS, HS>::THREADS, plan.smem_bytes, s>>>(
-        tm_k, tm_v, a);
+    decode_bf16_kernel<D, BS, HS, CONTIG>
+        <<<plan.ctas, Geom<D, BS, HS>::THREADS, plan.smem_bytes, s>>>(tm_k, tm_v, a);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }
 
@@ -730,17 +747,18 @@ int launch_bf16(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &
 // shared-memory limit; later calls read the cached answer, so the per-call
 // host cost of a decode launch is a few table lookups.
 constexpr int kMaxDev = 64;
-int g_occ_cache[kMaxDev][2][2][4];
+int g_occ_cache[kMaxDev][2][2][2][4];
 
-template <int D, int BS, int HS>
+template <int D, int BS, int HS, bool CONTIG>
 int occupancy_of(size_t smem)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-    int &slot = g_occ_cache[dev][D == 128][BS == 32][HS == 8 ? 3 : HS == 4 ? 2 : HS == 2 ? 1 : 0];
+    int &slot =
+        g_occ_cache[dev][CONTIG][D == 128][BS == 32][HS == 8 ? 3 : HS == 4 ? 2 : HS == 2 ? 1 : 0];
     const int cached = __atomic_load_n(&slot, __ATOMIC_ACQUIRE);
     if (cached > 0) return cached;
-    auto kern = decode_bf16_kernel<D, BS, HS>;
+    auto kern = decode_bf16_kernel<D, BS, HS, CONTIG>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return 0;
@@ -754,36 +772,37 @@ int occupancy_of(size_t smem)
 
 }  // namespace
 
-#define PA_DECODE_SWITCH(D_, BS_, HS_, ...)                                                  \
+// Runs __VA_ARGS__ with constexpr D, BS, HS set to the runtime values.
+#define PA_DECODE_HS(D_, BS_, HS_, ...)                                                      \
     do {                                                                                      \
-        if (D_ == 128 && BS_ == 16) {                                                         \
-            if (HS_ == 8) { constexpr int D = 128, BS = 16, HS = 8; __VA_ARGS__; }                   \
-            if (HS_ == 4) { constexpr int D = 128, BS = 16, HS = 4; __VA_ARGS__; }                   \
-            if (HS_ == 2) { constexpr int D = 128, BS = 16, HS = 2; __VA_ARGS__; }                   \
-            if (HS_ == 1) { constexpr int D = 128, BS = 16, HS = 1; __VA_ARGS__; }                   \
-        } else if (D_ == 128 && BS_ == 32) {                                                  \
-            if (HS_ == 8) { constexpr int D = 128, BS = 32, HS = 8; __VA_ARGS__; }                   \
-            if (HS_ == 4) { constexpr int D = 128, BS = 32, HS = 4; __VA_ARGS__; }                   \
-            if (HS_ == 2) { constexpr int D = 128, BS = 32, HS = 2; __VA_ARGS__; }                   \
-            if (HS_ == 1) { constexpr int D = 128, BS = 32, HS = 1; __VA_ARGS__; }                   \
-        } else if (D_ == 64 && BS_ == 16) {                                                   \
-            if (HS_ == 8) { constexpr int D = 64, BS = 16, HS = 8; __VA_ARGS__; }                    \
-            if (HS_ == 4) { constexpr int D = 64, BS = 16, HS = 4; __VA_ARGS__; }                    \
-            if (HS_ == 2) { constexpr int D = 64, BS = 16, HS = 2; __VA_ARGS__; }                    \
-            if (HS_ == 1) { constexpr int D = 64, BS = 16, HS = 1; __VA_ARGS__; }                    \
-        } else if (D_ == 64 && BS_ == 32) {                                                   \
-            if (HS_ == 8) { constexpr int D = 64, BS = 32, HS = 8; __VA_ARGS__; }                    \
-            if (HS_ == 4) { constexpr int D = 64, BS = 32, HS = 4; __VA_ARGS__; }                    \
-            if (HS_ == 2) { constexpr int D = 64, BS = 32, HS = 2; __VA_ARGS__; }                    \
-            if (HS_ == 1) { constexpr int D = 64, BS = 32, HS = 1; __VA_ARGS__; }                    \
+        if (HS_ == 8) { constexpr int D = D_, BS = BS_, HS = 8; __VA_ARGS__; }               \
+        if (HS_ == 4) { constexpr int D = D_, BS = BS_, HS = 4; __VA_ARGS__; }               \
+        if (HS_ == 2) { constexpr int D = D_, BS = BS_, HS = 2; __VA_ARGS__; }               \
+        if (HS_ == 1) { constexpr int D = D_, BS = BS_, HS = 1; __VA_ARGS__; }               \
+    } while (0)
+// Paged kernels: every supported (head_dim, block_size).  Contiguous-cache
+// kernels: only the unit contig_unit(head_dim).
+#define PA_DECODE_SWITCH(CONTIG_, D_, BS_, HS_, ...)                                         \
+    do {                                                                                      \
+        if (CONTIG_) {                                                                        \
+            constexpr bool CONTIG = true;                                                     \
+            if (D_ == 128 && BS_ == contig_unit(128)) PA_DECODE_HS(128, contig_unit(128), HS_, __VA_ARGS__); \
+            else if (D_ == 64 && BS_ == contig_unit(64)) PA_DECODE_HS(64, contig_unit(64), HS_, __VA_ARGS__); \
+        } else {                                                                              \
+            constexpr bool CONTIG = false;                                                    \
+            if (D_ == 128 && BS_ == 16) PA_DECODE_HS(128, 16, HS_, __VA_ARGS__);             \
+            else if (D_ == 128 && BS_ == 32) PA_DECODE_HS(128, 32, HS_, __VA_ARGS__);        \
+            else if (D_ == 64 && BS_ == 16) PA_DECODE_HS(64, 16, HS_, __VA_ARGS__);          \
+            else if (D_ == 64 && BS_ == 32) PA_DECODE_HS(64, 32, HS_, __VA_ARGS__);          \
         }                                                                                     \
     } while (0)
 
 int decode_bf16_plan(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                     DecodePlan *plan)
+                     DecodePlan *plan, bool contig)
 {
     if (!((head_dim == 64 || head_dim == 128) && (block_size == 16 || block_size == 32)))
         return PA_ERR_UNSUPPORTED;
+    if (contig && block_size != contig_unit(head_dim)) return PA_ERR_UNSUPPORTED;
     if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
     const int G = num_heads / num_kv_heads;
     if (G > 8) return PA_ERR_UNSUPPORTED;
@@ -797,7 +816,8 @@ int decode_bf16_plan(int batch, int num_heads, int num_kv_heads, int head_dim, i
     plan->nstages = nst;
     plan->smem_bytes = nst * stage + 1024 + (size_t)nst * 20 + 64;
     int occ = 0;
-    PA_DECODE_SWITCH(head_dim, block_size, hs, { occ = occupancy_of<D, BS, HS>(plan->smem_bytes); });
+    PA_DECODE_SWITCH(contig, head_dim, block_size, hs,
+                     { occ = occupancy_of<D, BS, HS, CONTIG>(plan->smem_bytes); });
     if (occ <= 0) return PA_ERR_LAUNCH;
     const int sms = num_sms();
     if (sms <= 0) return PA_ERR_DEVICE;
@@ -815,11 +835,12 @@ size_t decode_workspace_bytes(const DecodePlan &plan)
 }
 
 int decode_bf16_launch(const DecodeArgs &a, int head_dim, int block_size, const DecodePlan &plan,
-                       const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t s)
+                       const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t s,
+                       bool contig)
 {
     int rc = PA_ERR_UNSUPPORTED;
-    PA_DECODE_SWITCH(head_dim, block_size, plan.heads_per_cta,
-                     { rc = launch_bf16<D, BS, HS>(a, plan, tm_k, tm_v, s); });
+    PA_DECODE_SWITCH(contig, head_dim, block_size, plan.heads_per_cta,
+                     { rc = launch_bf16<D, BS, HS, CONTIG>(a, plan, tm_k, tm_v, s); });
     return rc;
 }
 

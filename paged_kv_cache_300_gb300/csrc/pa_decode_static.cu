@@ -56,8 +56,14 @@ extern "C" int pa_decode_static_scratch(const void *q, void *k_cache, void *v_ca
         return PA_ERR_SHAPE;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (batch == 0) return PA_OK;
+    // every check pa_decode makes on the host comes first: a call refused
+    // with a status must not have cleared the counters of a call in flight
+    if (!block_table || !cache_seqlens) return PA_ERR_NULL;
+    int rc = decode_check_pointers(q, k_cache, v_cache, k_new, v_new, out);
+    if (rc != PA_OK) return rc;
+    if ((long long)num_blocks * block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     DecodePlan plan;
-    int rc = decode_bf16_plan(batch, num_heads, num_kv_heads, head_dim, block_size, &plan);
+    rc = decode_bf16_plan(batch, num_heads, num_kv_heads, head_dim, block_size, &plan);
     if (rc != PA_OK) return rc;
     const size_t need = decode_workspace_bytes(plan);
     if (need > kStaticScratchBytes) return PA_ERR_WORKSPACE; // beyond the fixed maximum

@@ -24,6 +24,7 @@ struct DecodeArgs {
     int32_t *tickets; // per (sequence, kv head) arrival counters (bf16 path)
     int32_t *dev_err;
     int batch, num_heads, num_kv_heads, num_blocks, max_blocks_per_seq;
+    int max_seqlen;  // contiguous cache: rows per sequence (paged: unused)
     int group;       // num_heads / num_kv_heads
     int head_groups; // num_kv_heads / kv heads per CTA
     int nstages;
@@ -48,11 +49,21 @@ struct DecodePlan {
 // stays valid for calls of any shape; the split-K partials follow it.
 constexpr size_t kTicketRegionBytes = size_t(1) << 20;
 
+// `contig`: the kernel variant over a contiguous cache [batch, max_seqlen,
+// Hkv, D] with no block table (block_size is then its unit of tokens).
 int decode_bf16_plan(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                     DecodePlan *plan);
+                     DecodePlan *plan, bool contig = false);
 size_t decode_workspace_bytes(const DecodePlan &plan);
 int decode_bf16_launch(const DecodeArgs &a, int head_dim, int block_size, const DecodePlan &plan,
-                       const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t s);
+                       const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t s,
+                       bool contig = false);
+// Tokens per work unit of the contiguous decode variant: 16 for head_dim 128,
+// 32 for head_dim 64 (a 64 KB ring stage for 8 kv heads either way).
+constexpr int contig_unit(int head_dim) { return head_dim == 128 ? 16 : 32; }
+// Host checks shared by the decode entry points: PA_OK, or the status the
+// call must return before anything is launched.
+int decode_check_pointers(const void *q, const void *k_cache, const void *v_cache,
+                          const void *k_new, const void *v_new, const void *out);
 int decode_f32_launch(const DecodeArgs &a, int head_dim, int block_size, cudaStream_t s);
 
 // ------------------------------------------------------------------ cache update
@@ -98,6 +109,14 @@ struct VarlenArgs {
 // rows, key/value tiles 64 rows.
 constexpr int kVarlenQRows = 128;
 constexpr int kVarlenKRows = 64;
+// The CTA-pair kernel (tcgen05 cta_group::2): 128 query rows per CTA, S tiles
+// of 128 keys; a CTA loads K boxes of 64 keys and V boxes of 128 keys.
+constexpr int kVarlenPairKeys = 128;
+int varlen_pair_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                            const CUtensorMap &tm_v, cudaStream_t s);
+int varlen_pair_paged_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q,
+                                  const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                  cudaStream_t s);
 int varlen_f32_launch(const VarlenArgs &a, cudaStream_t s);
 int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                        const CUtensorMap &tm_v, cudaStream_t s);
@@ -108,6 +127,8 @@ int varlen_paged_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q,
 int num_sms();
 int encode_rows_map(CUtensorMap *map, const void *base, uint64_t rows, int heads, int head_dim,
                     int box_rows);
+int encode_unit_map(CUtensorMap *map, const void *base, uint64_t rows, int heads, int head_dim,
+                    int box_rows, int box_heads);
 int encode_packed_q_map(CUtensorMap *map, const void *base, uint64_t rows, int heads, int pack,
                         int box_queries);
 int varlen_pack_factor(int num_heads, int num_kv_heads);

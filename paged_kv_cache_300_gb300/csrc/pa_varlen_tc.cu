@@ -475,6 +475,44 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
             // P row (bf16 pairs) over the S_j row it came from; PV_j reads it
             // as the TMEM A operand.  Its own buffer: no wait on PV_{j-1}.
             tmem_st32(trow + st * BN, pk);
+            // The key tile that holds the request's last key also holds rows
+            // that are not keys of this request: the unwritten tail of a pool
+            // block (paged keys; any bits at all, NaN included) or the next
+            // request's rows.  Their weights are 0, but the tensor core
+            // multiplies 0 by whatever is there and 0 * NaN is NaN, so their
+            // V rows are zeroed before P V_j may start (rows whose whole block
+            // lies past the keys were zero-filled by the TMA already).
+            if (j == n_tiles - 1 && kl - kb < BN) {
+                const int z0 = kl - kb;
+                const int z1 = PAGED ? min(BN, (kl + a.block_size - 1) / a.block_size * a.block_size - kb)
+                                     : BN;
+                uint64_t *vbar;
+                uint32_t vpar;
+                uint8_t *vt;
+                if constexpr (PAGED) {
+                    vbar = &bar->v_full[st];
+                    vpar = (j >> 1) & 1;
+                    vt = smem + OFF_KV + (NSTAGE + st) * KV_BYTES;
+                } else {
+                    const int ti = j + 1; // V_j travels in transaction T_(j+1)
+                    vbar = &bar->kv_full[ti & 1];
+                    vpar = (ti >> 1) & 1;
+                    vt = smem + OFF_KV + (ti & 1) * STAGE_BYTES;
+                }
+                if (z1 > z0) {
+                    if (!mbar_wait(vbar, vpar)) {
+                        ok = false;
+                        break;
+                    }
+                    const int per_half = (z1 - z0) * 8; // 16-byte chunks per 64-dim half
+                    for (int c = r; c < 2 * per_half; c += BM) {
+                        const int hf = c / per_half, rem = c % per_half;
+                        *reinterpret_cast<uint4 *>(vt + hf * KBOX + (z0 + rem / 8) * 128 + (rem % 8) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+            }
             // O is rescaled only by a warp with a row whose max grew past the
             // threshold, after PV_{j-1} is done and before PV_j (which needs
             // this warp's arrival).  Otherwise P_j is released at once and
@@ -554,12 +592,17 @@ int launch_varlen(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMa
 {
     if (a.head_dim != HD) return PA_ERR_UNSUPPORTED;
     if (a.max_q <= 0) return PA_OK;
-    static bool attr_set = false; // one process-wide attribute per kernel
-    if (!attr_set) {
+    // the shared-memory limit is an attribute of the kernel in each device's
+    // context: raise it once per device
+    constexpr int kMaxDev = 64;
+    static int attr_set[kMaxDev] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return PA_ERR_DEVICE;
+    if (__atomic_load_n(&attr_set[dev], __ATOMIC_ACQUIRE) == 0) {
         if (cudaFuncSetAttribute(varlen_tc_kernel<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES) != cudaSuccess)
             return PA_ERR_LAUNCH;
-        attr_set = true;
+        __atomic_store_n(&attr_set[dev], 1, __ATOMIC_RELEASE);
     }
     const int qpt = BM / a.pack;
     const unsigned tiles = (unsigned)((a.max_q + qpt - 1) / qpt);

@@ -17,18 +17,32 @@ def tol_for(dtype):
     return BF16_TOL if dtype == torch.bfloat16 else F32_TOL
 
 
-def assert_close(gpu: torch.Tensor, ref: np.ndarray, dtype, what=""):
-    """|gpu - ref| <= tol + tol * |ref| element by element."""
+def assert_close(gpu: torch.Tensor, ref: np.ndarray, dtype, what="", discriminating=True):
+    """|gpu - ref| <= tol * s + tol * |ref| element by element, with
+    s = min(1, max|ref|): the pages' absolute-plus-relative bound, with the
+    absolute part scaled down to the output's own size when the outputs are
+    small, so that a comparison of tiny outputs still tests something.
+
+    With `discriminating` (the default) the check also proves it can fail:
+    an all-zero output must fall outside the bound somewhere, else the test
+    itself is rejected (a case whose reference is all zeros passes False)."""
     tol = tol_for(dtype)
     g = gpu.detach().float().cpu().numpy().astype(np.float64)
+    assert g.shape == ref.shape, f"{what}: shape {g.shape} vs {ref.shape}"
+    assert np.isfinite(g).all(), f"{what}: non-finite values in the GPU output"
+    scale = min(1.0, float(np.abs(ref).max())) if ref.size else 1.0
     err = np.abs(g - ref)
-    bound = tol + tol * np.abs(ref)
+    bound = tol * scale + tol * np.abs(ref)
+    if discriminating and ref.size:
+        assert (np.abs(ref) > bound).any(), (
+            f"{what}: the check cannot fail (an all-zero output would pass)")
     bad = err > bound
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(
             f"{what}: {int(bad.sum())} of {bad.size} elements outside tolerance "
-            f"(max abs err {err.max():.3e}); first {idx.tolist()}")
+            f"(max abs err {err.max():.3e}, max |ref| {np.abs(ref).max():.3e}); first "
+            f"{idx.tolist()}")
     return float(err.max()), float((err / np.maximum(np.abs(ref), 1e-30)).max())
 
 
@@ -60,3 +74,11 @@ def oracle_decode(case, rows=None):
 
 def bits(t: torch.Tensor) -> np.ndarray:
     return to_numpy(t.cpu())
+
+
+def same_bits(a: np.ndarray, b: np.ndarray) -> bool:
+    """Bitwise equality of two element arrays (NaN patterns included)."""
+    if a.shape != b.shape or a.dtype.itemsize != b.dtype.itemsize:
+        return False
+    u = {2: np.uint16, 4: np.uint32, 8: np.uint64}[a.dtype.itemsize]
+    return np.array_equal(np.ascontiguousarray(a).view(u), np.ascontiguousarray(b).view(u))

@@ -97,3 +97,33 @@ def test_binding_refuses_cpu_tensors():
     t = torch.zeros(1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         pa.pa_decode(t, t, t, t, t, t, t)
+
+
+def test_contiguous_decode_rejects_misuse_before_any_launch(lib):
+    P = ctypes.c_void_p
+    one = P(4096)
+
+    def call(q=one, sl=one, batch=1, hq=8, hkv=2, d=128, lmax=64, ws=None):
+        return lib.pa_decode_contiguous(q, one, one, sl, one, one, one, batch, hq, hkv, d, lmax,
+                                        0.0, ws, 0, None, None)
+    assert call(batch=0, q=None) == 0           # empty batch: nothing to do
+    assert call(q=None) == -1                   # PA_ERR_NULL
+    assert call(sl=None) == -1
+    assert call(d=96) == -4                     # PA_ERR_UNSUPPORTED
+    assert call(hq=6, hkv=4) == -3              # PA_ERR_SHAPE
+    assert call(lmax=0) == -3
+    assert call(q=P(4096 + 8)) == -3            # q not 16-byte aligned
+
+
+def test_static_scratch_checks_pointers_before_touching_its_counters(lib):
+    """A call refused for a null or misaligned pointer returns before it
+    looks up or clears the library's scratch (no CUDA call at all: this
+    machine may have no GPU)."""
+    P = ctypes.c_void_p
+    one = P(4096)
+    rc = lib.pa_decode_static_scratch(one, one, one, one, one, one, one, None, 1, 8, 2, 128, 8,
+                                      16, 4, 0.0, None, None)
+    assert rc == -1
+    rc = lib.pa_decode_static_scratch(P(4096 + 4), one, one, one, one, one, one, one, 1, 8, 2, 128,
+                                      8, 16, 4, 0.0, None, None)
+    assert rc == -3

@@ -151,3 +151,67 @@ def test_paged_pack_factors(heads):
     o = oracle.varlen(to_numpy(c.q), bits(kf), bits(vf), c.cu_seq_lens_q.numpy(),
                       c.cu_seq_lens_k.numpy(), True)
     assert_close(fused, o, torch.bfloat16, f"paged varlen, {hq}/{hkv} heads")
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
+@pytest.mark.parametrize("causal", [True, False])
+def test_paged_nan_in_unowned_pool_slots(bs, causal):
+    """Every pool slot that holds no cached key (unused blocks, the tail of
+    each request's last block, and the chunk slots before the scatter) holds
+    NaN.  The keys past a request's length in its last block are read by the
+    tile loads but weigh 0; the output must match the oracle (which reads
+    only the request's keys), hold no NaN, and equal the gather path bit for
+    bit."""
+    c = make_varlen(50 + bs, [1, 129, 300, 64, 255, 7, 0, 33],
+                    [0, 17, 300, 5, 130, 513, 40, 3], 8, 2, 128, bs, causal=causal)
+    c.poison_unowned()
+    fused, ref, kf, vf = _both_paths(c, causal)
+    assert not torch.isnan(fused.float()).any()
+    assert torch.equal(fused.view(torch.int16), ref.view(torch.int16))
+    o = oracle.varlen(to_numpy(c.q), bits(kf), bits(vf), c.cu_seq_lens_q.numpy(),
+                      c.cu_seq_lens_k.numpy(), causal)
+    assert_close(fused, o, torch.bfloat16, f"NaN-poisoned pool, bs={bs} causal={causal}")
+
+
+def test_mixed_batch_with_nan_in_unowned_pool_slots():
+    """The continuous-batching step of test_mixed_decode_and_prefill_in_one_launch
+    on a pool whose unwritten slots hold NaN."""
+    q_lens = [1, 200, 1, 1, 57, 1]
+    prefix = [300, 0, 17, 130, 400, 0]
+    c = make_varlen(22, q_lens, prefix, 8, 2, 128, 16)
+    c.poison_unowned()
+    t = lambda x: x.to("cuda")
+    kc, vc = t(c.k_cache), t(c.v_cache)
+    cq, bt, pl = t(c.cu_seq_lens_q), t(c.block_table), t(c.prefix_lens)
+    pa.pa_cache_update(t(c.k_chunk), t(c.v_chunk), cq, pl, bt, kc, vc)
+    seqlens_k = (c.cu_seq_lens_k[1:] - c.cu_seq_lens_k[:-1]).to(torch.int32).cuda()
+    mixed = pa.pa_varlen_paged(t(c.q), kc, vc, bt, cq, seqlens_k, c.max_length_q,
+                               c.max_length_k, True)
+    torch.cuda.synchronize()
+    assert not torch.isnan(mixed.float()).any()
+    kf, vf = oracle.cache_update(to_numpy(c.k_chunk), to_numpy(c.v_chunk), c.cu_seq_lens_q.numpy(),
+                                 c.prefix_lens.numpy(), c.block_table.numpy(),
+                                 to_numpy(c.k_cache).copy(), to_numpy(c.v_cache).copy(),
+                                 c.cu_seq_lens_k.numpy())
+    ref = oracle.varlen(to_numpy(c.q), kf, vf, c.cu_seq_lens_q.numpy(), c.cu_seq_lens_k.numpy(),
+                        True)
+    assert_close(mixed, ref, torch.bfloat16, "mixed batch, NaN-poisoned pool")
+
+
+def test_varlen_packed_keys_next_request_nan():
+    """Packed (gathered) keys: a request's last key tile reads the next
+    request's rows; NaN there (a request whose own output is then NaN) must
+    not reach the earlier request's output."""
+    gen = torch.Generator().manual_seed(5)
+    ql, kl = [40, 10], [70, 30]
+    cu_q = torch.tensor([0, 40, 50], dtype=torch.int32)
+    cu_k = torch.tensor([0, 70, 100], dtype=torch.int32)
+    q = torch.randn(50, 8, 128, generator=gen).to(torch.bfloat16)
+    k = torch.randn(100, 2, 128, generator=gen).to(torch.bfloat16)
+    v = torch.randn(100, 2, 128, generator=gen).to(torch.bfloat16)
+    k[70:], v[70:] = float("nan"), float("nan")
+    out = pa.pa_varlen(q.cuda(), k.cuda(), v.cuda(), cu_q.cuda(), cu_k.cuda(), 40, 70, True)
+    torch.cuda.synchronize()
+    ref = oracle.varlen(to_numpy(q[:40]), to_numpy(k[:70]), to_numpy(v[:70]),
+                        np.array([0, 40], np.int32), np.array([0, 70], np.int32), True)
+    assert_close(out[:40], ref, torch.bfloat16, "request 0 next to a NaN request")

@@ -118,6 +118,46 @@ class DecodeCase:
         return (2 * b * self.num_heads * self.head_dim + 4 * b * self.num_kv_heads *
                 self.head_dim) * e
 
+    def poison_unowned(self, value: float = float("nan")) -> "DecodeCase":
+        """Fill every pool slot that holds none of the cached positions
+        0..L_b-1 of any sequence with `value` (NaN by default): unused
+        blocks, the tails of last blocks and the append slots, i.e. what a
+        serving pool allocated with uninitialised memory may hold there.  The
+        attended values are unchanged (the append slot is written before it
+        is read).  In place; returns self."""
+        bs = self.block_size
+        tab = self.block_table.numpy()
+        owned = np.zeros(self.num_blocks * bs, dtype=bool)
+        for b, L in enumerate(self.cache_seqlens.tolist()):
+            pos = np.arange(L)
+            owned[tab[b, pos // bs].astype(np.int64) * bs + pos % bs] = True
+        free = torch.from_numpy(~owned).view(self.num_blocks, bs)
+        self.k_cache[free] = value
+        self.v_cache[free] = value
+        return self
+
+    def contiguous_cache(self, max_seqlen=None, fill: float = float("nan"), device="cpu"):
+        """The same logical K and V as a contiguous cache [B, max_seqlen,
+        Hkv, D] (the input of the contiguous-cache decode twin): row b holds
+        sequence b's cached positions 0..L_b-1, copied from the pool blocks
+        its table names, and `fill` everywhere else.  Returns (k, v) on
+        `device`."""
+        bs = self.block_size
+        L = self.cache_seqlens.to(torch.int64)
+        lmax = int(max_seqlen or int(L.max()) + 1)
+        pos = torch.arange(lmax)
+        tab = self.block_table.to(torch.int64)
+        blk = tab.gather(1, (pos // bs).clamp(max=tab.shape[1] - 1).expand(self.batch, -1))
+        valid = pos.unsqueeze(0) < L.unsqueeze(1)
+        rows = torch.where(valid, blk * bs + pos % bs, torch.zeros_like(blk)).reshape(-1)
+        out = []
+        for pool in (self.k_cache, self.v_cache):
+            flat = pool.reshape(-1, self.num_kv_heads, self.head_dim).to(device)
+            c = flat[rows.to(device)].reshape(self.batch, lmax, self.num_kv_heads, self.head_dim)
+            c[~valid.to(device)] = fill
+            out.append(c.contiguous())
+        return out[0], out[1]
+
     def permuted(self, seed: int) -> "DecodeCase":
         """Same logical content with the physical blocks renumbered by a
         random permutation pi: block p moves to pi[p]."""
@@ -229,6 +269,23 @@ class VarlenCase:
     def batch(self):
         return len(self.prefix_lens)
 
+    def poison_unowned(self, value: float = float("nan")) -> "VarlenCase":
+        """Fill every pool slot that holds no cached prefix position of any
+        request with `value` (NaN by default): the slots the chunk will be
+        scattered into, the tails of last blocks and unused blocks.  In
+        place; returns self."""
+        bs = self.k_cache.shape[1]
+        nb = self.k_cache.shape[0]
+        tab = self.block_table.numpy()
+        owned = np.zeros(nb * bs, dtype=bool)
+        for r, L in enumerate(self.prefix_lens.tolist()):
+            pos = np.arange(L)
+            owned[tab[r, pos // bs].astype(np.int64) * bs + pos % bs] = True
+        free = torch.from_numpy(~owned).view(nb, bs)
+        self.k_cache[free] = value
+        self.v_cache[free] = value
+        return self
+
     def causal_pairs(self) -> int:
         """(query, key) pairs the bottom-right causal mask keeps."""
         cq = self.cu_seq_lens_q.tolist()
@@ -281,12 +338,14 @@ WORKED_EXAMPLE_SEQLENS = [30, 32, 70]
 
 
 def decode_config(idx: int, scale_down: int = 1, seed_offset: int = 0,
-                  contiguous: bool = False) -> DecodeCase:
+                  contiguous: bool = False, unit_variance: bool = False) -> DecodeCase:
     """Decode workloads 1, 2, 3 and 5.  `scale_down` > 1 keeps the structure
     (heads, head_dim, block size, length distribution) with fewer sequences,
     for oracle runs that must finish in seconds.  `seed_offset` draws another
     batch of the same workload (one per rank when the benchmark runs on
-    several GPUs)."""
+    several GPUs).  `unit_variance` draws workload 2's values N(0,1) instead
+    of N(0,1)/sqrt(128): the same shapes with outputs large enough that a
+    wrong result cannot hide under the absolute tolerance."""
     seed = 1000 + idx + 100 * seed_offset
     if idx == 1:
         return make_decode(seed, WORKED_EXAMPLE_SEQLENS, 4, 2, 64, 32, dtype=torch.float32,
@@ -295,8 +354,10 @@ def decode_config(idx: int, scale_down: int = 1, seed_offset: int = 0,
     if idx == 2:
         b = max(1, 64 // scale_down)
         lengths = torch.randint(512, 4097, (b,), generator=g).tolist()
-        return make_decode(seed, lengths, 32, 8, 128, 16, value_scale=1.0 / math.sqrt(128.0),
-                           name=CONFIG_NAMES[2] + (" (blocks contiguous)" if contiguous else ""),
+        vs = 1.0 if unit_variance else 1.0 / math.sqrt(128.0)
+        name = CONFIG_NAMES[2] + (" (blocks contiguous)" if contiguous else "") + (
+            " (values N(0,1))" if unit_variance else "")
+        return make_decode(seed, lengths, 32, 8, 128, 16, value_scale=vs, name=name,
                            contiguous=contiguous)
     if idx == 3:
         b = max(1, 256 // scale_down)
