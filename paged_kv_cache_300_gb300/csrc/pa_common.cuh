@@ -13,11 +13,11 @@
 namespace pa {
 
 // Upper bound on polls of one mbarrier phase before a wait gives up.  Each
-// poll is an mbarrier.try_wait that suspends for up to kWaitSuspendNs, so
-// this is at most a few seconds of wall time: far beyond any legitimate
-// wait, short enough that a broken pipeline returns with PA_DEVERR_TIMEOUT
-// instead of hanging.
-constexpr uint32_t kWaitPolls = 1u << 24;
+// poll is an mbarrier.try_wait with a short suspend hint; an unsuccessful
+// poll measured about 4 us on GB300, so this bound is a few seconds of wall
+// time: far beyond any legitimate wait (microseconds), short enough that a
+// broken pipeline returns with PA_DEVERR_TIMEOUT instead of hanging.
+constexpr uint32_t kWaitPolls = 1u << 20;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -289,127 +289,5 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// ---------------------------------------------------------------- CTA pairs
-// Helpers of the kernels that run as clusters of two CTAs, one per SM of a
-// pair, and issue tcgen05.mma.cta_group::2: the even CTA issues every MMA of
-// the pair; operands come from the same shared-memory offsets of both CTAs,
-// and each CTA's tensor memory holds its own 128 rows of the result.
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// shared::cluster address of the same shared-memory offset in CTA `rank`
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-
-// Arrive on an mbarrier of any CTA of the cluster (address from mapa_shared),
-// releasing this thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
-
-// Wait on a local mbarrier whose arrivals may come from the other CTA of the
-// pair: acquire at cluster scope.  Bounded like mbar_wait.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitSuspendNs)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity)
-{
-    for (uint32_t i = 0; i < kWaitPolls; ++i)
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-    return false;
-}
-
-// Warp-uniform forms: every lane polls, and the warp agrees on the result,
-// so that a timeout seen by one lane cannot split the warp.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity)
-{
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
-}
-
-__device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity)
-{
-    return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity));
-}
-
-// Every thread of both CTAs must execute this (it has no time limit): the
-// kernels reach it on every path, timeouts included.
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void umma2_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void umma2_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                  uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// One arrival on the mbarrier at this shared-memory offset in both CTAs of
-// the pair once every tcgen05 operation issued so far has completed.
-__device__ __forceinline__ void umma2_commit_both(uint64_t *bar)
-{
-    const uint16_t mask = 3;
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-// Executed by one warp in each CTA of the pair (collective): both receive
-// the same column address.
-__device__ __forceinline__ void tmem2_alloc(uint32_t *dst_smem, uint32_t ncols)
-{
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem2_dealloc(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
 
 }  // namespace pa

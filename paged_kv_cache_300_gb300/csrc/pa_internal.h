@@ -109,14 +109,6 @@ struct VarlenArgs {
 // rows, key/value tiles 64 rows.
 constexpr int kVarlenQRows = 128;
 constexpr int kVarlenKRows = 64;
-// The CTA-pair kernel (tcgen05 cta_group::2): 128 query rows per CTA, S tiles
-// of 128 keys; a CTA loads K boxes of 64 keys and V boxes of 128 keys.
-constexpr int kVarlenPairKeys = 128;
-int varlen_pair_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                            const CUtensorMap &tm_v, cudaStream_t s);
-int varlen_pair_paged_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q,
-                                  const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                                  cudaStream_t s);
 int varlen_f32_launch(const VarlenArgs &a, cudaStream_t s);
 int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                        const CUtensorMap &tm_v, cudaStream_t s);
