@@ -120,6 +120,15 @@ size_t pa_decode_workspace_size(int batch, int num_heads, int num_kv_heads, int 
  *               workspace must be ordered on the GPU.  batch * num_kv_heads
  *               may not exceed 262144 (PA_ERR_UNSUPPORTED).
  * Result is independent of where the blocks sit in the pool (bitwise).
+ *
+ * Host buffers: q, block_table, cache_seqlens, k_new, v_new and out may be
+ * page-locked host memory (cudaHostAlloc / cudaMallocHost, or
+ * cudaHostRegister-ed), passed as the host pointer.  GB300 reaches such
+ * memory in place over NVLink-C2C (unified addressing), so the kernel reads
+ * the step's inputs and writes its output there during the call, with no
+ * separate copy; a caller that keeps its per-step tensors on the host saves
+ * two transfers per step.  k_cache, v_cache, workspace and dev_err must be
+ * device memory.  The caller reads `out` after the stream reaches the call.
  */
 int pa_decode(const void *q, void *k_cache, void *v_cache, const int32_t *block_table,
               const int32_t *cache_seqlens, const void *k_new, const void *v_new, void *out,

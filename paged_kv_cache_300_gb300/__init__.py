@@ -124,6 +124,21 @@ def _check_dev(*ts):
     return dev
 
 
+def _check_host_or_dev(dev, *ts):
+    """Per-step tensors of pa_decode: on `dev`, or page-locked host memory
+    (which the kernel reads and writes in place over NVLink-C2C)."""
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+        if t.is_cuda:
+            if t.device != dev:
+                raise ValueError("all tensors must be on the same device")
+        elif not t.is_pinned():
+            raise ValueError("host tensors must be page-locked (pin_memory())")
+
+
 def _i32(t, name):
     if t is not None and t.dtype != torch.int32:
         raise TypeError(f"{name} must be int32")
@@ -162,9 +177,12 @@ def pa_decode(q, k_cache, v_cache, block_table, cache_seqlens, k_new, v_new, out
     """Decode step (see include/pa.h).  q [B, Hq, D]; k_cache/v_cache
     [NB, bs, Hkv, D] (the new token is written in place); block_table
     [B, MB] int32; cache_seqlens [B] int32; k_new/v_new [B, Hkv, D].
-    Returns out [B, Hq, D]."""
-    dev = _check_dev(q, k_cache, v_cache, block_table, cache_seqlens, k_new, v_new, out,
-                     workspace, dev_err)
+    Returns out [B, Hq, D].  q, block_table, cache_seqlens, k_new, v_new
+    and out may be pinned host tensors (read and written in place; `out`
+    defaults to a pinned host tensor then); the pools, workspace and
+    dev_err live on the GPU."""
+    dev = _check_dev(k_cache, v_cache, workspace, dev_err)
+    _check_host_or_dev(dev, q, block_table, cache_seqlens, k_new, v_new, out)
     _i32(block_table, "block_table")
     _i32(cache_seqlens, "cache_seqlens")
     _i32(dev_err, "dev_err")
@@ -179,7 +197,7 @@ def pa_decode(q, k_cache, v_cache, block_table, cache_seqlens, k_new, v_new, out
         raise ValueError("inconsistent shapes")
     mb = block_table.shape[1]
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty_like(q, pin_memory=not q.is_cuda)
     elif out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("out must match q")
     lib = load()

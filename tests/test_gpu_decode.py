@@ -197,3 +197,30 @@ def test_full_size_sampled(idx, unit_variance):
     for b in range(len(L)):
         p, s = tab[b, L[b] // case.block_size], L[b] % case.block_size
         assert np.array_equal(kcb[p, s], knb[b])
+
+
+def test_host_buffers_read_and_written_in_place():
+    """q, block_table, cache_seqlens, k_new, v_new and out in page-locked host
+    memory: the kernel reads and writes them in place (NVLink-C2C); the
+    result equals the device-buffer call bit for bit, the append lands in
+    the device pool, and the output matches the oracle."""
+    case = decode_config(2, scale_down=8, unit_variance=True)
+    dev_out, dev_k, dev_v = gpu_decode(case)
+    kc, vc = case.k_cache.cuda(), case.v_cache.cuda()
+    pin = lambda x: x.clone().pin_memory()
+    host = [pin(x) for x in (case.q, case.block_table, case.cache_seqlens, case.k_new, case.v_new)]
+    out = pa.pa_decode(host[0], kc, vc, host[1], host[2], host[3], host[4])
+    torch.cuda.synchronize()
+    assert not out.is_cuda and out.is_pinned()
+    assert torch.equal(out.view(torch.int16), dev_out.cpu().view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), dev_k.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), dev_v.view(torch.int16))
+    ref, _, _ = oracle_decode(case)
+    assert_close(out, ref, torch.bfloat16, "host buffers")
+
+
+def test_unpinned_host_tensors_are_refused():
+    case = make_decode(2, [10, 20], 8, 2, 64, 16)
+    with pytest.raises(ValueError):
+        pa.pa_decode(case.q, case.k_cache.cuda(), case.v_cache.cuda(), case.block_table.cuda(),
+                     case.cache_seqlens.cuda(), case.k_new.cuda(), case.v_new.cuda())
