@@ -115,6 +115,21 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream is still
+// running; grid_dep_wait() returns once that kernel has finished and its
+// writes are visible, so nothing a predecessor may write is read before it.
+// grid_dep_trigger() lets the kernel after this one start as this grid's
+// CTAs leave their SMs.  Both are no-ops for a launch without the attribute.
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Byte offset of element (row, col) inside a TMA box whose rows are 128
 // bytes of 16-bit elements (64 per row) loaded with 128-byte swizzling: the
 // 16-byte chunk index is XORed with row % 8.  Boxes start 1024-byte aligned.

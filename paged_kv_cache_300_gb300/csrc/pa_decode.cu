@@ -161,10 +161,20 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
     }
+    // The next kernel on the stream (when it was launched for programmatic
+    // dependence, e.g. the next decode step) is launched once every CTA of
+    // this grid has passed here, so it never takes an SM one of ours still
+    // needs; its CTAs take SMs as ours leave them and run their own start-up
+    // during this grid's merge tail, then wait for this grid to finish.
+    grid_dep_trigger();
+    // L2 prefetches are hints, and L2 is where every write lands, so they may
+    // run before the predecessor has finished: a line it rewrites later is
+    // simply updated.  The lengths are prefetched for the scan below, and a
+    // small block table, each CTA taking a slice, so that the producer's
+    // first table read after the scan hits in L2 instead of waiting on HBM.
+    for (int b = tid * 32; b < B; b += NT * 32)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.cache_seqlens + b));
     if constexpr (!CONTIG) {
-        // A small block table is brought into L2 now, each CTA taking a
-        // slice, so that the producer's first table read after the length
-        // scan below hits in L2 instead of waiting on HBM.
         const size_t tbytes = (size_t)B * mbps * 4;
         if (tbytes <= ((size_t)4 << 20)) {
             const size_t lines = (tbytes + 127) / 128;
@@ -174,6 +184,8 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(tb + l * 128));
         }
     }
+    // Nothing above read or wrote memory a predecessor may write.
+    grid_dep_wait();
 
     // ---- block-wide exclusive scan of the per-sequence block counts
     const int per = (B + NT - 1) / NT;
@@ -736,10 +748,22 @@ template <int D, int BS, int HS, bool CONTIG>
 int launch_bf16(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &tm_k,
                 const CUtensorMap &tm_v, cudaStream_t s)
 {
-    // the shared-memory attribute was set when the plan was made
-    decode_bf16_kernel<D, BS, HS, CONTIG>
-        <<<plan.ctas, Geom<D, BS, HS>::THREADS, plan.smem_bytes, s>>>(tm_k, tm_v, a);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+    // The shared-memory attribute was set when the plan was made.  The
+    // launch allows programmatic dependence: the kernel's start-up (barrier
+    // set-up, descriptor and L2 prefetches) may overlap the end of the kernel
+    // before it on the stream, and it reads nothing before that kernel is done.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.ctas);
+    cfg.blockDim = dim3(Geom<D, BS, HS>::THREADS);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_bf16_kernel<D, BS, HS, CONTIG>, tm_k, tm_v, a);
+    return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }
 
 // Resident CTAs per SM of one instantiation on the current device.  The

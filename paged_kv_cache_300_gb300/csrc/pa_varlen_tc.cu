@@ -225,10 +225,30 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
         return;
     }
 
-    if (tid == 0) {
+    // The K loader thread sets up the barriers of its first loads itself and
+    // issues them now (Q; contiguous keys: also T_0 = {K_0, K_1}), so that
+    // their latency overlaps the TMEM allocation and the block-wide barrier
+    // below; every other thread touches those barriers only after that
+    // barrier.
+    const bool k_lane = warp == 4 && lane == 0;
+    if (k_lane) {
         mbar_init(&bar->q_full, 1);
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar->kv_full[s], 1);
+        fence_mbar_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        mbar_arrive_expect_tx(&bar->q_full, Q_BYTES);
+        for (int c = 0; c < 2; ++c)
+            tma_load_4d(sbase + OFF_Q + c * QBOX, &tm_q, &bar->q_full, 0, c, h0, q0 + r0);
+        if constexpr (!PAGED) {
+            mbar_arrive_expect_tx(&bar->kv_full[0], min(2, n_tiles) * KV_BYTES);
+            for (int t = 0; t < min(2, n_tiles); ++t)
+                load_kv_tile<PAGED>(sbase + OFF_KV + t * KV_BYTES, &tm_k, &bar->kv_full[0], a, b,
+                                    kvh, k0, kl, t, nullptr, nullptr);
+        }
+    }
+    if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&bar->kv_full[s], 1);
             mbar_init(&bar->kv_empty[s], 1);
             mbar_init(&bar->v_full[s], 1);
             mbar_init(&bar->v_empty[s], 1);
@@ -263,18 +283,9 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
         // two threads load: one Q and the K tiles, the other the V tiles, so
         // that neither waits behind the other's issue loop (contiguous keys:
         // the K thread announces each transaction's bytes, V included)
-        const bool k_lane = warp == 4 && lane == 0;
         const bool v_lane = PAGED ? (warp == 6 && lane == 0) : (warp == 4 && lane == 1);
         if (k_lane || v_lane) {
-            if (k_lane) {
-                prefetch_tmap(&tm_q);
-                prefetch_tmap(&tm_k);
-                mbar_arrive_expect_tx(&bar->q_full, Q_BYTES);
-                for (int c = 0; c < 2; ++c)
-                    tma_load_4d(sbase + OFF_Q + c * QBOX, &tm_q, &bar->q_full, 0, c, h0, q0 + r0);
-            } else {
-                prefetch_tmap(&tm_v);
-            }
+            if (v_lane) prefetch_tmap(&tm_v);
             if constexpr (PAGED) {
                 // K ring (K thread) or V ring (V thread): stage j % 2 holds
                 // tile j and frees when the MMAs reading tile j - 2 are done
@@ -292,7 +303,8 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
                                         b, kvh, k0, kl, j, &bar->bad_block, tab);
                 }
             } else {
-                for (int i = 0; i <= n_tiles; ++i) {
+                // T_0 went out before the block-wide barrier
+                for (int i = k_lane ? 1 : 0; i <= n_tiles; ++i) {
                     const int st = i & 1;
                     // T_i's stage frees when the MMAs reading T_(i-2) are done
                     if (i >= NSTAGE && !mbar_wait(&bar->kv_empty[st], ((i >> 1) - 1) & 1)) {
@@ -302,17 +314,11 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
                     const uint32_t slot_a = sbase + OFF_KV + st * STAGE_BYTES;
                     const uint32_t slot_b = slot_a + KV_BYTES;
                     if (k_lane) {
-                        // announces the whole transaction: K tiles and V tile
-                        const int kb = i + 1; // K tile in slot B for i >= 1
-                        const int tiles = i == 0 ? min(2, n_tiles) : 1 + (kb < n_tiles ? 1 : 0);
+                        // announces the whole transaction: K tile and V tile
+                        const int kb = i + 1; // K tile in slot B
+                        const int tiles = 1 + (kb < n_tiles ? 1 : 0);
                         mbar_arrive_expect_tx(&bar->kv_full[st], tiles * KV_BYTES);
-                        if (i == 0) {
-                            load_kv_tile<PAGED>(slot_a, &tm_k, &bar->kv_full[st], a, b, kvh, k0, kl,
-                                                0, &bar->bad_block, tab);
-                            if (n_tiles > 1)
-                                load_kv_tile<PAGED>(slot_b, &tm_k, &bar->kv_full[st], a, b, kvh, k0,
-                                                    kl, 1, &bar->bad_block, tab);
-                        } else if (kb < n_tiles) {
+                        if (kb < n_tiles) {
                             load_kv_tile<PAGED>(slot_b, &tm_k, &bar->kv_full[st], a, b, kvh, k0, kl,
                                                 kb, &bar->bad_block, tab);
                         }

@@ -63,3 +63,72 @@ def test_block_manager_prefill_fork_decode():
     for s in seqs:
         bm.free(s)
     assert bm.num_free() == nb
+
+
+@pytest.mark.parametrize("mode", ["stream", "graph"])
+def test_back_to_back_steps_each_reading_the_last_append(mode):
+    """K decode steps launched back to back with no host synchronisation (on
+    one stream, or captured as one CUDA graph as the benchmark runs them),
+    step t attending over the token step t-1 appended and sharing one
+    workspace.  Each launch allows programmatic dependence, so a step's
+    start-up overlaps the previous step; every output and both pools must
+    still equal the oracle run step by step."""
+    b, hq, hkv, d, bs, steps = 24, 32, 8, 128, 16, 6
+    g = torch.Generator().manual_seed(4242)
+    lens = torch.randint(200, 1500, (b,), generator=g)
+    mbps = (int(lens.max()) + steps + bs - 1) // bs
+    need = [(int(n) + steps + bs - 1) // bs for n in lens]
+    nb = sum(need) + 8
+    perm = torch.randperm(nb, generator=g)
+    table = torch.full((b, mbps), -1, dtype=torch.int32)
+    o = 0
+    for s in range(b):
+        table[s, :need[s]] = perm[o:o + need[s]]
+        o += need[s]
+    rnd = lambda *sh: torch.randn(*sh, generator=g).to(torch.bfloat16)
+    kc0, vc0 = rnd(nb, bs, hkv, d), rnd(nb, bs, hkv, d)
+    qs = [rnd(b, hq, d) for _ in range(steps)]
+    kns = [rnd(b, hkv, d) for _ in range(steps)]
+    vns = [rnd(b, hkv, d) for _ in range(steps)]
+    sls = [(lens + t).to(torch.int32) for t in range(steps)]
+    dev = "cuda"
+    kc, vc = kc0.to(dev), vc0.to(dev)
+    tab = table.to(dev)
+    dq = [x.to(dev) for x in qs]
+    dkn = [x.to(dev) for x in kns]
+    dvn = [x.to(dev) for x in vns]
+    dsl = [x.to(dev) for x in sls]
+    outs = [torch.empty(b, hq, d, dtype=torch.bfloat16, device=dev) for _ in range(steps)]
+    ws = torch.zeros(pa.pa_decode_workspace_size(b, hq, hkv, d, bs), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run_all():
+        for t in range(steps):
+            pa.pa_decode(dq[t], kc, vc, tab, dsl[t], dkn[t], dvn[t], outs[t], workspace=ws,
+                         dev_err=err)
+
+    if mode == "graph":
+        run_all()  # first calls outside capture (plan and descriptor set-up)
+        torch.cuda.synchronize()
+        kc.copy_(kc0)
+        vc.copy_(vc0)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run_all()
+        torch.cuda.synchronize()
+        kc.copy_(kc0)
+        vc.copy_(vc0)
+        for x in outs:
+            x.zero_()
+        torch.cuda.synchronize()
+        graph.replay()
+    else:
+        run_all()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rk, rv = bits(kc0).copy(), bits(vc0).copy()
+    for t in range(steps):
+        ref = oracle.decode(bits(qs[t]), rk, rv, table.numpy(), sls[t].numpy(), bits(kns[t]),
+                            bits(vns[t]))
+        assert_close(outs[t], ref, torch.bfloat16, f"{mode} step {t}")
+    assert np.array_equal(bits(kc), rk) and np.array_equal(bits(vc), rv)
