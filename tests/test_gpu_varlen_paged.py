@@ -77,9 +77,13 @@ def test_paged_invariant_to_block_placement():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def test_paged_missing_block_flags_and_zeroes():
+@pytest.mark.parametrize("missing", [2, 8])
+def test_paged_missing_block_flags_and_zeroes(missing):
+    """A needed -1 entry of request 0: block 2 (positions 32..47, in the
+    first key tile, loaded before the block-wide barrier) or block 8
+    (positions 128..143, in the third tile, loaded by the ring loop)."""
     c = make_varlen(4, [50, 60], [100, 20], 8, 2, 128, 16)
-    c.block_table[0, 2] = -1  # a needed block of request 0 (positions 32..47)
+    c.block_table[0, missing] = -1
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     t = lambda x: x.to("cuda")
     seqlens_k = (c.cu_seq_lens_k[1:] - c.cu_seq_lens_k[:-1]).to(torch.int32)
