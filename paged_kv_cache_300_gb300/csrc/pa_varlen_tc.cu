@@ -177,6 +177,13 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
     const int m = gridDim.y - 1 - blockIdx.y; // heavy (late) tiles first
     const int G = a.num_heads / a.num_kv_heads, kvh = h0 / G;
 
+    // Paged keys: the loader warps read the first 32 entries of the
+    // request's table row now, alongside the length loads below, so that the
+    // first tiles' boxes do not wait for a table round trip of their own.
+    int tab_head = -1;
+    if (PAGED && (warp == 4 || warp == 6) && lane < a.max_blocks_per_seq)
+        tab_head = __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + lane);
+
     const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
     int k0 = 0, kl = 0;
     bool bad_cu = q0 < 0 || q1 < q0 || q1 > a.total_q || q1 - q0 > (int)gridDim.y * QPT;
@@ -268,9 +275,11 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
         // each loader warp stages its own copy of the table slice
         int *tab = reinterpret_cast<int *>(smem + OFF_TAB + (warp == 6 ? 4 * TAB_CAP : 0));
         if constexpr (PAGED) {
-            // stage this CTA's slice of the block table (coalesced, once)
+            // stage this CTA's slice of the block table (coalesced, once; the
+            // first 32 entries were read at entry)
             const int need = min(TAB_CAP, (min(kl, n_tiles * BN) + a.block_size - 1) / a.block_size);
-            for (int e = lane; e < need; e += 32)
+            if (lane < need) tab[lane] = tab_head;
+            for (int e = 32 + lane; e < need; e += 32)
                 tab[e] = __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
             __syncwarp();
         }
@@ -290,7 +299,10 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
             const CUtensorMap *map = kw ? &tm_k : &tm_v;
             const int nbox = 2 * (BN / a.block_size);
             for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
+                const int st = j & 1, i = lane >> 1, c = lane & 1;
+                // the box's pool row is looked up before the stage is waited
+                // for, so that a freed stage is refilled at once
+                const int row = lane < nbox ? paged_row(a, b, kl, j, i, tab, &bar->bad_block) : 0;
                 int go = 1;
                 if (j >= NSTAGE && lane == 0) go = mbar_wait(&empty[st], ((j >> 1) - 1) & 1);
                 if (!__shfl_sync(0xffffffffu, go, 0)) {
@@ -299,11 +311,9 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
                 }
                 if (lane == 0) mbar_arrive_expect_tx(&full[st], KV_BYTES);
                 __syncwarp();
-                if (lane < nbox) {
-                    const int i = lane >> 1, c = lane & 1;
+                if (lane < nbox)
                     tma_load_3d(ring + st * KV_BYTES + c * KBOX + i * a.block_size * 128, map, &full[st],
-                                0, kvh * 2 + c, paged_row(a, b, kl, j, i, tab, &bar->bad_block));
-                }
+                                0, kvh * 2 + c, row);
             }
         } else {
             // Contiguous keys: two threads load, one the K tiles (it announces
