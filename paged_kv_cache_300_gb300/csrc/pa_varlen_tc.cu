@@ -464,7 +464,8 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
                 for (int c = 0; c < BN; ++c)
                     if (kb + c > lim) s[c] = -INFINITY;
             }
-            // row max as 8 independent chains (short critical path)
+            // row max as 8 independent chains (short critical path; four
+            // chains of the three-input max measured slower)
             float mx8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mx8[u] = s[u];
@@ -482,16 +483,20 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
                 m_run = m_new;
             }
             const float mu = m_run == -INFINITY ? 0.f : m_run;
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f}; // 4 independent partial sums
+            // the scale-and-offset and the running sums take the paired fp32
+            // instructions (two lanes of arithmetic per instruction): the
+            // softmax phase is issue-bound, not bound by the exponentials
+            const float2 sl2x2 = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
+            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}; // 4 partial sums
             uint32_t pk[BN / 2];
 #pragma unroll
             for (int c = 0; c < BN; c += 2) {
-                const float p0 = exp2_approx(fmaf(s[c], sl2, -mu));
-                const float p1 = exp2_approx(fmaf(s[c + 1], sl2, -mu));
-                sum4[(c >> 1) & 3] += p0 + p1;
+                const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2x2, nmu);
+                const float p0 = exp2_approx(x.x), p1 = exp2_approx(x.y);
+                sum2[(c >> 1) & 1] = __fadd2_rn(sum2[(c >> 1) & 1], make_float2(p0, p1));
                 pk[c >> 1] = pack_bf16(p0, p1);
             }
-            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+            const float sum = (sum2[0].x + sum2[1].x) + (sum2[0].y + sum2[1].y);
             l_run = l_run * alpha + sum;
             // P row (bf16 pairs) over the S_j row it came from; PV_j reads it
             // as the TMEM A operand.  Its own buffer: no wait on PV_{j-1}.
