@@ -418,7 +418,12 @@ int pa_varlen(const void *q, const void *k, const void *v, const int32_t *cu_seq
         tm_k = tm_q;
         tm_v = tm_q;
     }
-    return varlen_bf16_launch(a, tm_q, tm_k, tm_v, s);
+    // the output has q's layout; full tiles are stored through the same kind
+    // of box (an out pointer that is not 16-byte aligned takes thread stores)
+    CUtensorMap tm_o = tm_q;
+    a.out_tma = cached_map(&tm_o, 2, out, (uint64_t)total_q, num_heads, a.pack, kVarlenQRows / a.pack,
+                           0) == PA_OK;
+    return varlen_bf16_launch(a, tm_q, tm_k, tm_v, tm_o, s);
 }
 
 int pa_varlen_paged(const void *q, const void *k_cache, const void *v_cache,
@@ -472,7 +477,10 @@ int pa_varlen_paged(const void *q, const void *k_cache, const void *v_cache,
         return rc;
     if ((rc = cached_map(&tm_v, 0, v_cache, rows, num_kv_heads, head_dim, block_size, 0)) != PA_OK)
         return rc;
-    return varlen_paged_bf16_launch(a, tm_q, tm_k, tm_v, static_cast<cudaStream_t>(stream));
+    CUtensorMap tm_o = tm_q;
+    a.out_tma = cached_map(&tm_o, 2, out, (uint64_t)total_q, num_heads, a.pack, kVarlenQRows / a.pack,
+                           0) == PA_OK;
+    return varlen_paged_bf16_launch(a, tm_q, tm_k, tm_v, tm_o, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

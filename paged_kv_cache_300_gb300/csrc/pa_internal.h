@@ -104,6 +104,9 @@ struct VarlenArgs {
     // tensor-core kernel: query heads packed per 128-row tile (a power of two
     // dividing num_heads / num_kv_heads); a tile holds 128 / pack queries
     int pack;
+    // 1 when the output tensor map was encoded, so that full tiles leave
+    // through a TMA store
+    int out_tma;
 };
 // Rows of one TMA box of the tensor-core varlen kernel: query tiles are 128
 // rows, key/value tiles 64 rows.
@@ -111,9 +114,10 @@ constexpr int kVarlenQRows = 128;
 constexpr int kVarlenKRows = 64;
 int varlen_f32_launch(const VarlenArgs &a, cudaStream_t s);
 int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                       const CUtensorMap &tm_v, cudaStream_t s);
+                       const CUtensorMap &tm_v, const CUtensorMap &tm_o, cudaStream_t s);
 int varlen_paged_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q,
-                             const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t s);
+                             const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                             const CUtensorMap &tm_o, cudaStream_t s);
 
 // ------------------------------------------------------------------ helpers
 int num_sms();

@@ -102,6 +102,7 @@ struct Barriers {
     uint64_t p_full[2];
     uint64_t o_done;   // one phase per PV_j (waited only before an O rescale)
     uint64_t all_done; // one phase: every MMA of the CTA has completed
+    uint64_t o_staged; // one phase: the four softmax warps wrote the output tile to smem
     uint32_t tmem_base;
     int bad_block; // paged variant: a needed table entry was not a valid block
 };
@@ -161,7 +162,8 @@ __device__ __forceinline__ int paged_row(const VarlenArgs &a, int b, int kl, int
 template <bool PAGED>
 __global__ void __launch_bounds__(kThreads<PAGED>, 2)
     varlen_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const VarlenArgs a)
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                     const VarlenArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -260,6 +262,7 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
         mbar_init(&bar->p_full[1], 4);
         mbar_init(&bar->o_done, 1);
         mbar_init(&bar->all_done, 1);
+        mbar_init(&bar->o_staged, 4);
         bar->bad_block = 0;
         fence_mbar_init();
     }
@@ -575,20 +578,58 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
         if (ok && mbar_wait(&bar->all_done, 0)) {
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            uint4 *orow = reinterpret_cast<uint4 *>(out + out_row(r));
+            if (a.out_tma && rows_here == BM) {
+                // A full tile leaves through the TMA: every thread writes its
+                // bf16 row into the Q buffer (no MMA reads it any more) in
+                // the layout the Q load used, and one thread stores the two
+                // 64-dim boxes.  Thread stores of 16-byte pieces of 128
+                // different rows took ~1.5 us of the ~1.8 us epilogue.
+                uint8_t *qs = smem + OFF_Q;
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(trow + COL_O + c * 32, o);
-                tmem_ld_wait();
-                if (r < rows_here) {
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(trow + COL_O + c * 32, o);
+                    tmem_ld_wait();
+                    uint8_t *box = qs + (c >> 1) * QBOX + r * 128;
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8)
-                        orow[(c * 32 + e) / 8] = make_uint4(
+                    for (int e = 0; e < 32; e += 8) {
+                        const int chunk = ((c & 1) * 32 + e) >> 3; // 16-byte chunk in the 128-byte row
+                        *reinterpret_cast<uint4 *>(box + ((chunk ^ (r & 7)) << 4)) = make_uint4(
                             pack_bf16(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
                             pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
                             pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
                             pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->o_staged);
+                if (r == 0) {
+                    if (mbar_wait(&bar->o_staged, 0)) {
+                        for (int c = 0; c < 2; ++c)
+                            tma_store_4d(&tm_o, sbase + OFF_Q + c * QBOX, 0, c, h0, q0 + r0);
+                        bulk_commit();
+                        bulk_wait_read(); // the Q buffer is read before the CTA leaves
+                    } else {
+                        ok = false;
+                    }
+                }
+            } else {
+                uint4 *orow = reinterpret_cast<uint4 *>(out + out_row(r));
+    #pragma unroll
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(trow + COL_O + c * 32, o);
+                    tmem_ld_wait();
+                    if (r < rows_here) {
+    #pragma unroll
+                        for (int e = 0; e < 32; e += 8)
+                            orow[(c * 32 + e) / 8] = make_uint4(
+                                pack_bf16(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
+                                pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                                pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                                pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+                    }
                 }
             }
         } else {
@@ -601,9 +642,15 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
     tc_fence_after();
     if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
     if constexpr (PAGED) {
-        // a needed block was missing: flag it and zero the tile's rows
+        // a needed block was missing: flag it and zero the tile's rows (after
+        // the tile's TMA store, if it took one, has written them: thread 0
+        // issued it)
         if (bar->bad_block) {
-            if (tid == 0) flag_error(a.dev_err, PA_DEVERR_BAD_BLOCK);
+            if (tid == 0) {
+                flag_error(a.dev_err, PA_DEVERR_BAD_BLOCK);
+                bulk_wait_all_global();
+            }
+            __syncthreads();
             if (tid < rows_here) {
                 uint4 *o = reinterpret_cast<uint4 *>(out + out_row(tid));
                 for (int c = 0; c < HD / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -614,7 +661,7 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
 
 template <bool PAGED>
 int launch_varlen(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                  const CUtensorMap &tm_v, cudaStream_t s)
+                  const CUtensorMap &tm_v, const CUtensorMap &tm_o, cudaStream_t s)
 {
     if (a.head_dim != HD) return PA_ERR_UNSUPPORTED;
     if (a.max_q <= 0) return PA_OK;
@@ -634,22 +681,23 @@ int launch_varlen(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMa
     const unsigned tiles = (unsigned)((a.max_q + qpt - 1) / qpt);
     if (tiles > 65535u || a.batch > 65535) return PA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)(a.num_heads / a.pack), tiles, (unsigned)a.batch);
-    varlen_tc_kernel<PAGED><<<grid, kThreads<PAGED>, SMEM_BYTES, s>>>(tm_q, tm_k, tm_v, a);
+    varlen_tc_kernel<PAGED><<<grid, kThreads<PAGED>, SMEM_BYTES, s>>>(tm_q, tm_k, tm_v, tm_o, a);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }
 
 }  // namespace
 
 int varlen_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                       const CUtensorMap &tm_v, cudaStream_t s)
+                       const CUtensorMap &tm_v, const CUtensorMap &tm_o, cudaStream_t s)
 {
-    return launch_varlen<false>(a, tm_q, tm_k, tm_v, s);
+    return launch_varlen<false>(a, tm_q, tm_k, tm_v, tm_o, s);
 }
 
 int varlen_paged_bf16_launch(const VarlenArgs &a, const CUtensorMap &tm_q,
-                             const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t s)
+                             const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                             const CUtensorMap &tm_o, cudaStream_t s)
 {
-    return launch_varlen<true>(a, tm_q, tm_k, tm_v, s);
+    return launch_varlen<true>(a, tm_q, tm_k, tm_v, tm_o, s);
 }
 
 }  // namespace pa
