@@ -419,7 +419,7 @@ int pa_varlen(const void *q, const void *k, const void *v, const int32_t *cu_seq
         tm_v = tm_q;
     }
     // the output has q's layout; full tiles are stored through the same kind
-    // of box (an out pointer that is not 16-byte aligned takes thread stores)
+    // of box (should the map fail to encode, every tile takes thread stores)
     CUtensorMap tm_o = tm_q;
     a.out_tma = cached_map(&tm_o, 2, out, (uint64_t)total_q, num_heads, a.pack, kVarlenQRows / a.pack,
                            0) == PA_OK;
