@@ -575,7 +575,13 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
                         pml[g0 * 2 + 3] = bad ? -1.f : l1;
                     }
                 }
-                __threadfence();
+                // The warp's partial writes are ordered before lane 0's ticket
+                // increment by the warp barrier, and the increment is an
+                // acquire-release at GPU scope: it publishes them, and the
+                // last arriver acquires every other segment's partial through
+                // it (then the warp barrier orders its lanes' loads after
+                // that).  One round trip instead of a fence in every lane
+                // before the increment and another after it.
                 __syncwarp();
                 int last = 0;
                 int32_t *ticket = a.tickets + (size_t)w.b * Hkv + kvh;
@@ -584,10 +590,14 @@ __global__ void __launch_bounds__((HS + 1) * 32, 1)
                 // sequence has exactly nblk segments, one per unit
                 const bool dense = U >= P;
                 const int nseg = dense ? clast - cfirst + 1 : w.nblk;
-                if (lane == 0) last = atomicAdd(ticket, 1) == nseg - 1;
+                if (lane == 0) {
+                    int old;
+                    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(ticket) : "memory");
+                    last = old == nseg - 1;
+                }
                 last = __shfl_sync(kFull, last, 0);
                 if (last) {
-                    __threadfence();
+                    __syncwarp();
                     // fold the partials in logical (CTA) order.  Each
                     // partial's (m, l) and accumulator rows for every head of
                     // the group are loaded together before any of them is
