@@ -31,10 +31,10 @@
 //              Contiguous keys: lane 0 loads the K tiles of 64 keys (two 64-dim
 //              swizzled boxes each) and lane 1 the V tiles, into one ring whose
 //              stage i % 2 holds {V_(i-1), K_(i+1)} as a single TMA transaction
-//              (see NSTAGE below).  Paged keys: a tile is one box per pool
-//              block and 64-dim half; warp 4 fills a K ring and warp 6 a V
-//              ring, one box per lane; a K stage frees as soon as S_j = Q K_j^T
-//              is computed, a V stage when O += P_j V_j is.
+//              (see NSTAGE below).  Paged keys: the same ring, but a tile is
+//              one box per pool block and 64-dim half, and warps 4, 6 and 7
+//              (6 only, for blocks of 32 or 64 keys) share each transaction's
+//              boxes, one box per lane.
 //   warp 5     TMEM allocator and MMA issuer (one thread): S_j = Q K_j^T into
 //              one of two TMEM S buffers (M=128, N=64, K=16 per instruction,
 //              both operands K-major from shared memory), then O += P_j V_j
@@ -66,38 +66,42 @@ constexpr int KV_BYTES = 2 * KBOX;            // one K (or V) tile of 64 keys
 // of S_(i+1), which the MMA thread issues back to back.  One transaction of
 // two tiles instead of one per tile halves the TMA transactions per key (a
 // TMA transaction costs a few hundred cycles whatever its size, and the
-// per-tile rings kept the SM's TMA unit busy all the time).  Paged keys take
-// one box per block, so there the cost is per box, not per transaction, and
-// the same 64 KB hold a K ring and a V ring of two 16 KB stages each
-// (K_j's stage frees when S_j is done, V_j's when P V_j is), filled by two
-// warps: V tiles then go out earlier than the K tiles of the same step, and
-// the two box streams are issued in parallel (one ring of {V_(i-1), K_(i+1)}
-// transactions, one box per lane of one warp, measured 0.79 ms against
-// 0.68 ms at block size 16 on the prefill workload).
+// per-tile rings kept the SM's TMA unit busy all the time; giving V its own
+// barrier in the same ring measured 4.6% slower on the prefill workload).
+// Paged keys use the same transactions, each filled by two or three warps
+// that issue in parallel, one box per lane (one warp issuing all 16 boxes at
+// block size 16 measured 0.79 ms against 0.68 ms for two; a K ring and a V
+// ring, each with its own warp and barriers, measured 1.5% slower at block
+// size 16 and 4.1% at block size 64).
 constexpr int NSTAGE = 2;
 constexpr int STAGE_BYTES = 2 * KV_BYTES;     // slot A (V, or K_0) + slot B (K)
 constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + Q_BYTES;      // paged keys: K ring, then V ring
+constexpr int OFF_KV = OFF_Q + Q_BYTES;
 constexpr int OFF_BAR = OFF_KV + NSTAGE * STAGE_BYTES;
 constexpr int TAB_CAP = 512;                  // block-table entries staged in smem (paged)
 constexpr int OFF_TAB = OFF_BAR + 256;
-// two staged copies of the table slice (one per loader warp), + alignment
+// three staged copies of the table slice (one per loader warp), + alignment
 // slack: still two CTAs per SM
-constexpr int SMEM_BYTES = OFF_TAB + 2 * 4 * TAB_CAP + 1024;
+constexpr int SMEM_BYTES = OFF_TAB + 3 * 4 * TAB_CAP + 1024;
 // warps 0-3 softmax, 4 TMA (Q + K; contiguous keys: V too), 5 MMA; paged
-// keys: warp 6 loads the V ring, so neither ring waits behind the other's
-// issue loop
-template <bool PAGED> constexpr int kThreads = PAGED ? 224 : 192;
+// keys: warps 6 and 7 issue TMA boxes too, in parallel with warp 4 (a ninth
+// warp would cap the kernel below the registers the softmax needs at two
+// CTAs per SM)
+template <bool PAGED> constexpr int kThreads = PAGED ? 256 : 192;
+
+// Paged keys: the loader warps that share a transaction's boxes.  A warp
+// issues its lanes' boxes one after another, so with small blocks more warps
+// issue faster: 3 warps against 2 measured 0.690 -> 0.635 ms at block size 8
+// and 0.605 -> 0.602 at 16 on the prefill workload, but 0.582 -> 0.584 at 64.
+__device__ __forceinline__ int paged_loaders(int block_size) { return block_size <= 16 ? 3 : 2; }
 constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t COL_O = 2 * BN;
 constexpr float kRescaleThreshold = 8.0f; // log2 units
 
 struct Barriers {
     uint64_t q_full;
-    uint64_t kv_full[NSTAGE];  // the transaction (paged keys: the K ring)
+    uint64_t kv_full[NSTAGE];  // transaction T_i in stage i % 2 (paged keys: both loader warps arrive)
     uint64_t kv_empty[NSTAGE];
-    uint64_t v_full[NSTAGE];   // paged keys: the V ring
-    uint64_t v_empty[NSTAGE];
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t o_done;   // one phase per PV_j (waited only before an O rescale)
@@ -138,21 +142,19 @@ __device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap *ma
     for (int c = 0; c < 2; ++c) tma_load_3d(dst + c * KBOX, map, full, 0, kvh * 2 + c, k0 + j * BN);
 }
 
-// Pool row of block i of paged key tile j: the tile's keys are logical
-// positions 64 j .. 64 j + 63 of the request, i.e. 64 / block_size pool
-// blocks resolved through the block table (the staged slice `tab`, or the
-// table itself past TAB_CAP entries).  Each block's box lands at its row
-// offset inside the tile (a multiple of 8 rows, so the 128-byte swizzle phase
-// is the same as for a packed tile).  Positions past the request's keys, and
-// needed entries that are not valid blocks (flagged), get a row past the end
-// of the pool, whose box reads the TMA's zero fill.
-__device__ __forceinline__ int paged_row(const VarlenArgs &a, int b, int kl, int j, int i,
+// Pool row of entry e of a request's block table: the entry covers the
+// request's key positions e bs .. e bs + bs - 1, and the box of key tile
+// j = e bs / 64 loads them into their row offset inside the tile (a multiple
+// of 8 rows, so the 128-byte swizzle phase is the same as for a packed tile).
+// The entry comes from the staged slice `tab`, or the table itself past
+// TAB_CAP entries.  An entry past the request's keys, and a needed entry that
+// is not a valid block (flagged), get a row past the end of the pool, whose
+// box reads the TMA's zero fill.
+__device__ __forceinline__ int paged_row(const VarlenArgs &a, int b, int kl, int e,
                                          const int *tab, int *bad_block)
 {
     const int bs = a.block_size;
-    const int pos = j * BN + i * bs;
-    if (pos >= kl) return a.num_blocks * bs;
-    const int e = pos / bs;
+    if (e * bs >= kl) return a.num_blocks * bs;
     const int p = e < TAB_CAP ? tab[e] : __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
     if (p >= 0 && p < a.num_blocks) return p * bs;
     *bad_block = 1;
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
     // request's table row now, alongside the length loads below, so that the
     // first tiles' boxes do not wait for a table round trip of their own.
     int tab_head = -1;
-    if (PAGED && (warp == 4 || warp == 6) && lane < a.max_blocks_per_seq)
+    if (PAGED && (warp == 4 || warp >= 6) && lane < a.max_blocks_per_seq)
         tab_head = __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + lane);
 
     const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
@@ -228,34 +230,53 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
         return;
     }
 
-    // The K loader thread sets up the barriers of its first loads itself and
-    // issues them now (Q; contiguous keys: also T_0 = {K_0, K_1}), so that
-    // their latency overlaps the TMEM allocation and the block-wide barrier
-    // below; every other thread touches those barriers only after that
-    // barrier.  (For paged keys, issuing the first two tiles of both rings
-    // here too, each lane reading its own table entry, measured no faster.)
+    // The K loader sets up the barriers of its first loads itself and issues
+    // them now (Q and T_0 = {K_0, K_1}), so that their latency overlaps the
+    // TMEM allocation and the block-wide barrier below; every other thread
+    // touches those barriers only after that barrier.  Paged keys: the whole
+    // warp issues T_0's boxes, one per lane, each reading its pool block from
+    // the table entries read at entry (T_0 issued after the barrier reached
+    // the MMA thread ~700 cycles later per CTA at block size 64, ~1300 at 16).
     const bool k_lane = warp == 4 && lane == 0;
-    if (k_lane) {
-        mbar_init(&bar->q_full, 1);
-        for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar->kv_full[s], 1);
-        fence_mbar_init();
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        mbar_arrive_expect_tx(&bar->q_full, Q_BYTES);
-        for (int c = 0; c < 2; ++c)
-            tma_load_4d(sbase + OFF_Q + c * QBOX, &tm_q, &bar->q_full, 0, c, h0, q0 + r0);
-        if constexpr (!PAGED) {
+    if (warp == 4) {
+        if (k_lane) {
+            mbar_init(&bar->q_full, 1);
+            for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar->kv_full[s], PAGED ? paged_loaders(a.block_size) : 1);
+            bar->bad_block = 0;
+            fence_mbar_init();
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            mbar_arrive_expect_tx(&bar->q_full, Q_BYTES);
+            for (int c = 0; c < 2; ++c)
+                tma_load_4d(sbase + OFF_Q + c * QBOX, &tm_q, &bar->q_full, 0, c, h0, q0 + r0);
             mbar_arrive_expect_tx(&bar->kv_full[0], min(2, n_tiles) * KV_BYTES);
-            for (int t = 0; t < min(2, n_tiles); ++t)
-                load_kv_tile(sbase + OFF_KV + t * KV_BYTES, &tm_k, &bar->kv_full[0], kvh, k0, t);
+            if constexpr (!PAGED)
+                for (int t = 0; t < min(2, n_tiles); ++t)
+                    load_kv_tile(sbase + OFF_KV + t * KV_BYTES, &tm_k, &bar->kv_full[0], kvh, k0, t);
+        }
+        if constexpr (PAGED) {
+            // lane 2 i + c (+ one tile's boxes for K_1): the 64-dim half c of
+            // pool block i of the tile; entry e < 2 * (64 / block_size) <= 16
+            const int bpt = BN / a.block_size, nbox = 2 * bpt;
+            const int tt = lane / nbox, rem = lane % nbox, blk = rem >> 1, c = rem & 1;
+            const int e = tt * bpt + blk;
+            const int p = __shfl_sync(0xffffffffu, tab_head, e & 31);
+            __syncwarp(); // the barrier init and the byte count come first
+            if (tt < min(2, n_tiles)) {
+                int row = a.num_blocks * a.block_size; // past the keys: zero fill
+                if (e * a.block_size < kl) {
+                    if (p >= 0 && p < a.num_blocks)
+                        row = p * a.block_size;
+                    else
+                        bar->bad_block = 1;
+                }
+                tma_load_3d(sbase + OFF_KV + tt * KV_BYTES + c * KBOX + blk * a.block_size * 128, &tm_k,
+                            &bar->kv_full[0], 0, kvh * 2 + c, row);
+            }
         }
     }
     if (tid == 0) {
-        for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&bar->kv_empty[s], 1);
-            mbar_init(&bar->v_full[s], 1);
-            mbar_init(&bar->v_empty[s], 1);
-        }
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar->kv_empty[s], 1);
         mbar_init(&bar->s_full[0], 1);
         mbar_init(&bar->s_full[1], 1);
         mbar_init(&bar->p_full[0], 4);
@@ -263,7 +284,6 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
         mbar_init(&bar->o_done, 1);
         mbar_init(&bar->all_done, 1);
         mbar_init(&bar->o_staged, 4);
-        bar->bad_block = 0;
         fence_mbar_init();
     }
     if (warp == 5) tmem_alloc(&bar->tmem_base, TMEM_COLS);
@@ -273,50 +293,67 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
     const uint32_t tmem = bar->tmem_base;
     bool ok = true;
 
-    if (warp == 4 || warp == 6) {
+    if (warp == 4 || warp >= 6) {
         // ================= TMA producers =================
         // each loader warp stages its own copy of the table slice
-        int *tab = reinterpret_cast<int *>(smem + OFF_TAB + (warp == 6 ? 4 * TAB_CAP : 0));
+        const int w = warp == 4 ? 0 : warp - 5; // paged keys: loader 0, 1 or 2
+        int *tab = reinterpret_cast<int *>(smem + OFF_TAB + w * 4 * TAB_CAP);
         if constexpr (PAGED) {
-            // stage this CTA's slice of the block table (coalesced, once; the
-            // first 32 entries were read at entry)
-            const int need = min(TAB_CAP, (min(kl, n_tiles * BN) + a.block_size - 1) / a.block_size);
-            if (lane < need) tab[lane] = tab_head;
-            for (int e = 32 + lane; e < need; e += 32)
-                tab[e] = __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
-            __syncwarp();
-        }
-        if constexpr (PAGED) {
-            // K ring (warp 4) or V ring (warp 6): stage j % 2 holds tile j and
-            // frees when the MMAs reading tile j - 2 are done.  The whole
-            // warp issues a tile's boxes, one per lane: lane 2 i + c loads the
-            // 64-dim half c of the tile's pool block i.  A thread issues its
-            // TMA boxes one after another, and with 2 KB boxes (block size 16)
-            // a single issuing thread, not the TMA unit, set the loaders' pace
-            // (prefill workload: 0.92 -> 0.68 ms).
-            const bool kw = warp == 4;
-            if (!kw && lane == 0) prefetch_tmap(&tm_v);
-            uint64_t *full = kw ? bar->kv_full : bar->v_full;
-            uint64_t *empty = kw ? bar->kv_empty : bar->v_empty;
-            const uint32_t ring = sbase + OFF_KV + (kw ? 0 : NSTAGE * KV_BYTES);
-            const CUtensorMap *map = kw ? &tm_k : &tm_v;
-            const int nbox = 2 * (BN / a.block_size);
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1, i = lane >> 1, c = lane & 1;
-                // the box's pool row is looked up before the stage is waited
-                // for, so that a freed stage is refilled at once
-                const int row = lane < nbox ? paged_row(a, b, kl, j, i, tab, &bar->bad_block) : 0;
-                int go = 1;
-                if (j >= NSTAGE && lane == 0) go = mbar_wait(&empty[st], ((j >> 1) - 1) & 1);
-                if (!__shfl_sync(0xffffffffu, go, 0)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) mbar_arrive_expect_tx(&full[st], KV_BYTES);
+            // The loader warps fill transaction T_i of the ring above
+            // together (warp 4 issued T_0 = {K_0, K_1} alone, before the
+            // block-wide barrier): box g of T_i, counting V_(i-1)'s boxes
+            // (slot A) and then K_(i+1)'s (slot B), goes to loader g % W,
+            // lane g / W.  A tile has one box per pool block and 64-dim half:
+            // box 2 i + c of a tile loads the 64-dim half c of its block i.
+            // Each warp announces its own boxes' bytes, so the barrier takes
+            // W arrivals a phase.  With 2 KB boxes (block size 16) a single
+            // issuing thread, not the TMA unit, set the loaders' pace
+            // (prefill workload: 0.92 -> 0.68 ms with one box per lane).
+            const int W = paged_loaders(a.block_size);
+            if (w < W) {
+                // T_0 is warp 4's alone: the others' arrivals on it come
+                // first, ahead of the table reads (arriving after the table
+                // staging put its latency before T_0: ~750 cycles of MMA
+                // wait per CTA at block size 16 against ~290 for contiguous
+                // keys)
+                if (w > 0 && lane == 0) mbar_arrive(&bar->kv_full[0]);
+                if (w == 1 && lane == 0) prefetch_tmap(&tm_v);
+                const int bpt = BN / a.block_size, nbox = 2 * bpt;
+                // The table slice this CTA reads: the first 32 entries were
+                // read at entry and cover the boxes of T_0 and T_1 (at most 3
+                // tiles = 24 blocks of 8 keys); the rest is staged while those
+                // load.  (Staging pool rows, validated once, instead of block
+                // ids measured 0.4-1% slower.)
+                const int need = min(TAB_CAP, (min(kl, n_tiles * BN) + a.block_size - 1) / a.block_size);
+                if (lane < need) tab[lane] = tab_head;
                 __syncwarp();
-                if (lane < nbox)
-                    tma_load_3d(ring + st * KV_BYTES + c * KBOX + i * a.block_size * 128, map, &full[st],
-                                0, kvh * 2 + c, row);
+                const int g = lane * W + w;
+                const int tt = g / nbox, rem = g % nbox, blk = rem >> 1, c = rem & 1;
+                const CUtensorMap *map = tt == 0 ? &tm_v : &tm_k;
+                for (int i = 1; i <= n_tiles; ++i) {
+                    const int st = i & 1;
+                    if (i == NSTAGE) {
+                        for (int e = 32 + lane; e < need; e += 32)
+                            tab[e] = __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
+                        __syncwarp();
+                    }
+                    const int t = tt == 0 ? i - 1 : i + 1; // this lane's tile
+                    const bool mine = g < 2 * nbox && (tt == 0 || t < n_tiles);
+                    const int row = mine ? paged_row(a, b, kl, t * bpt + blk, tab, &bar->bad_block) : 0;
+                    const int nmine = __popc(__ballot_sync(0xffffffffu, mine));
+                    int go = 1;
+                    if (i >= NSTAGE && lane == 0) go = mbar_wait(&bar->kv_empty[st], ((i >> 1) - 1) & 1);
+                    if (!__shfl_sync(0xffffffffu, go, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(&bar->kv_full[st], nmine * a.block_size * 128);
+                    __syncwarp();
+                    if (mine)
+                        tma_load_3d(sbase + OFF_KV + st * STAGE_BYTES + tt * KV_BYTES + c * KBOX +
+                                        blk * a.block_size * 128,
+                                    map, &bar->kv_full[st], 0, kvh * 2 + c, row);
+                }
             }
         } else {
             // Contiguous keys: two threads load, one the K tiles (it announces
@@ -364,66 +401,35 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
                               idesc_qk, kk > 0);
                 umma_commit(&bar->s_full[sb]);
             };
-            // S_0 and S_1 go first; afterwards S_(j+2) is issued right after
-            // P V_j (which consumes P_j from the same TMEM columns; the tensor
-            // pipe executes one thread's MMAs in order)
-            if constexpr (PAGED) {
-                auto issue_qk_ring = [&](int j) -> bool {
-                    const int st = j & 1;
-                    if (!mbar_wait(&bar->kv_full[st], (j >> 1) & 1)) return false;
-                    tc_fence_after();
-                    issue_qk(j, sbase + OFF_KV + st * KV_BYTES);
-                    umma_commit(&bar->kv_empty[st]);
-                    return true;
-                };
-                if (ok) ok = issue_qk_ring(0);
-                if (ok && n_tiles > 1) ok = issue_qk_ring(1);
-                for (int j = 0; j < n_tiles && ok; ++j) {
-                    const int st = j & 1;
-                    if (!mbar_wait(&bar->p_full[st], (j >> 1) & 1) ||
-                        !mbar_wait(&bar->v_full[st], (j >> 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t pt = tmem + st * BN;
-                    const uint32_t vs = sbase + OFF_KV + (NSTAGE + st) * KV_BYTES;
+            // S_0 and S_1 (both from T_0) go first; afterwards P V_j and
+            // S_(j+2), both from T_(j+1), go back to back (P V_j reads P_j
+            // from the TMEM columns that S_(j+2) overwrites; the tensor pipe
+            // executes one thread's MMAs in order)
+            if (ok) ok = mbar_wait(&bar->kv_full[0], 0);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(0, sbase + OFF_KV);
+                if (n_tiles > 1) issue_qk(1, sbase + OFF_KV + KV_BYTES);
+                umma_commit(&bar->kv_empty[0]);
+            }
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int sb = j & 1, i = j + 1, st = i & 1;
+                if (!mbar_wait(&bar->p_full[sb], (j >> 1) & 1) ||
+                    !mbar_wait(&bar->kv_full[st], (i >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // P_j (bf16, 32 columns) overwrote the first half of S_j in TMEM
+                const uint32_t pt = tmem + sb * BN;
+                const uint32_t vs = sbase + OFF_KV + st * STAGE_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        umma_bf16_tmem_a(tmem + COL_O, pt + kk * 8, v_desc(vs, kk), idesc_pv,
-                                         (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&bar->o_done);
-                    umma_commit(&bar->v_empty[st]);
-                    if (j + 2 < n_tiles && !(ok = issue_qk_ring(j + 2))) break;
-                }
-            } else {
-                // S_0 and S_1 from T_0, then S_(j+2) and P V_j from T_(j+1)
-                if (ok) ok = mbar_wait(&bar->kv_full[0], 0);
-                if (ok) {
-                    tc_fence_after();
-                    issue_qk(0, sbase + OFF_KV);
-                    if (n_tiles > 1) issue_qk(1, sbase + OFF_KV + KV_BYTES);
-                    umma_commit(&bar->kv_empty[0]);
-                }
-                for (int j = 0; j < n_tiles && ok; ++j) {
-                    const int sb = j & 1, i = j + 1, st = i & 1;
-                    if (!mbar_wait(&bar->p_full[sb], (j >> 1) & 1) ||
-                        !mbar_wait(&bar->kv_full[st], (i >> 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // P_j (bf16, 32 columns) overwrote the first half of S_j in TMEM
-                    const uint32_t pt = tmem + sb * BN;
-                    const uint32_t vs = sbase + OFF_KV + st * STAGE_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        umma_bf16_tmem_a(tmem + COL_O, pt + kk * 8, v_desc(vs, kk), idesc_pv,
-                                         (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&bar->o_done);
-                    if (j + 2 < n_tiles) issue_qk(j + 2, vs + KV_BYTES);
-                    umma_commit(&bar->kv_empty[st]);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_bf16_tmem_a(tmem + COL_O, pt + kk * 8, v_desc(vs, kk), idesc_pv,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bar->o_done);
+                if (j + 2 < n_tiles) issue_qk(j + 2, vs + KV_BYTES);
+                umma_commit(&bar->kv_empty[st]);
             }
             if (ok) umma_commit(&bar->all_done); // tracks every MMA issued above
             // and the last o_done arrival lands before the CTA leaves (every
@@ -431,14 +437,8 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
             if (ok) ok = mbar_wait(&bar->all_done, 0) && mbar_wait(&bar->o_done, (n_tiles - 1) & 1);
             // the loaders never wait for the last two stage releases: wait
             // here so that no commit arrives after the CTA has left
-            if constexpr (PAGED) {
-                for (int t = max(0, n_tiles - 2); t < n_tiles && ok; ++t)
-                    ok = mbar_wait(&bar->kv_empty[t & 1], (t >> 1) & 1) &&
-                         mbar_wait(&bar->v_empty[t & 1], (t >> 1) & 1);
-            } else {
-                for (int t = max(0, n_tiles - 1); t <= n_tiles && ok; ++t)
-                    ok = mbar_wait(&bar->kv_empty[t & 1], (t >> 1) & 1);
-            }
+            for (int t = max(0, n_tiles - 1); t <= n_tiles && ok; ++t)
+                ok = mbar_wait(&bar->kv_empty[t & 1], (t >> 1) & 1);
         }
         __syncwarp();
     } else {
@@ -515,19 +515,10 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
                 const int z0 = kl - kb;
                 const int z1 = PAGED ? min(BN, (kl + a.block_size - 1) / a.block_size * a.block_size - kb)
                                      : BN;
-                uint64_t *vbar;
-                uint32_t vpar;
-                uint8_t *vt;
-                if constexpr (PAGED) {
-                    vbar = &bar->v_full[st];
-                    vpar = (j >> 1) & 1;
-                    vt = smem + OFF_KV + (NSTAGE + st) * KV_BYTES;
-                } else {
-                    const int ti = j + 1; // V_j travels in transaction T_(j+1)
-                    vbar = &bar->kv_full[ti & 1];
-                    vpar = (ti >> 1) & 1;
-                    vt = smem + OFF_KV + (ti & 1) * STAGE_BYTES;
-                }
+                const int ti = j + 1; // V_j travels in transaction T_(j+1)
+                uint64_t *vbar = &bar->kv_full[ti & 1];
+                const uint32_t vpar = (ti >> 1) & 1;
+                uint8_t *vt = smem + OFF_KV + (ti & 1) * STAGE_BYTES;
                 if (z1 > z0) {
                     if (!mbar_wait(vbar, vpar)) {
                         ok = false;
