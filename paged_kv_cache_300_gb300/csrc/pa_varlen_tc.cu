@@ -142,25 +142,6 @@ __device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap *ma
     for (int c = 0; c < 2; ++c) tma_load_3d(dst + c * KBOX, map, full, 0, kvh * 2 + c, k0 + j * BN);
 }
 
-// Pool row of entry e of a request's block table: the entry covers the
-// request's key positions e bs .. e bs + bs - 1, and the box of key tile
-// j = e bs / 64 loads them into their row offset inside the tile (a multiple
-// of 8 rows, so the 128-byte swizzle phase is the same as for a packed tile).
-// The entry comes from the staged slice `tab`, or the table itself past
-// TAB_CAP entries.  An entry past the request's keys, and a needed entry that
-// is not a valid block (flagged), get a row past the end of the pool, whose
-// box reads the TMA's zero fill.
-__device__ __forceinline__ int paged_row(const VarlenArgs &a, int b, int kl, int e,
-                                         const int *tab, int *bad_block)
-{
-    const int bs = a.block_size;
-    if (e * bs >= kl) return a.num_blocks * bs;
-    const int p = e < TAB_CAP ? tab[e] : __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
-    if (p >= 0 && p < a.num_blocks) return p * bs;
-    *bad_block = 1;
-    return a.num_blocks * bs;
-}
-
 template <bool PAGED>
 __global__ void __launch_bounds__(kThreads<PAGED>, 2)
     varlen_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -327,9 +308,25 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
                 const int need = min(TAB_CAP, (min(kl, n_tiles * BN) + a.block_size - 1) / a.block_size);
                 if (lane < need) tab[lane] = tab_head;
                 __syncwarp();
+                // This lane's box g: half c of block blk of the V tile
+                // (tt = 0, V_(i-1), slot A) or of the K tile (tt = 1,
+                // K_(i+1), slot B), landing at its row offset inside the tile
+                // (a multiple of 8 rows, so the 128-byte swizzle phase is the
+                // same as for a packed tile).  Its table entry at step i is
+                // e0 + i bpt; a V box loads at every step, a K box while
+                // K_(i+1) exists (i < ilim).
                 const int g = lane * W + w;
+                const bool gv = g < 2 * nbox;
                 const int tt = g / nbox, rem = g % nbox, blk = rem >> 1, c = rem & 1;
                 const CUtensorMap *map = tt == 0 ? &tm_v : &tm_k;
+                const uint32_t dst0 = sbase + OFF_KV + tt * KV_BYTES + c * KBOX + blk * a.block_size * 128;
+                const int e0 = tt == 0 ? blk - bpt : blk + bpt;
+                const int ilim = tt == 0 ? n_tiles + 1 : n_tiles - 1;
+                const int nblk = (kl + a.block_size - 1) / a.block_size; // entries holding keys
+                // a row past the end of the pool: its box reads the TMA's zero fill
+                const int oob = a.num_blocks * a.block_size;
+                const int vbytes = __popc(__ballot_sync(0xffffffffu, gv && tt == 0)) * a.block_size * 128;
+                const int kbytes = __popc(__ballot_sync(0xffffffffu, gv && tt == 1)) * a.block_size * 128;
                 for (int i = 1; i <= n_tiles; ++i) {
                     const int st = i & 1;
                     if (i == NSTAGE) {
@@ -337,22 +334,31 @@ __global__ void __launch_bounds__(kThreads<PAGED>, 2)
                             tab[e] = __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
                         __syncwarp();
                     }
-                    const int t = tt == 0 ? i - 1 : i + 1; // this lane's tile
-                    const bool mine = g < 2 * nbox && (tt == 0 || t < n_tiles);
-                    const int row = mine ? paged_row(a, b, kl, t * bpt + blk, tab, &bar->bad_block) : 0;
-                    const int nmine = __popc(__ballot_sync(0xffffffffu, mine));
+                    // The box's pool row.  Entries past the request's keys
+                    // load zeros; a needed entry that is not a valid block is
+                    // flagged and loads zeros.  A loaded tile's entries below
+                    // TAB_CAP are all staged; later ones come from the table.
+                    const int e = e0 + i * bpt;
+                    const bool mine = gv && i < ilim;
+                    int row = oob;
+                    if (mine && e < nblk) {
+                        const int p = e < TAB_CAP ? tab[e]
+                                                  : __ldg(a.block_table + (size_t)b * a.max_blocks_per_seq + e);
+                        if ((unsigned)p < (unsigned)a.num_blocks)
+                            row = p * a.block_size;
+                        else
+                            bar->bad_block = 1;
+                    }
                     int go = 1;
                     if (i >= NSTAGE && lane == 0) go = mbar_wait(&bar->kv_empty[st], ((i >> 1) - 1) & 1);
                     if (!__shfl_sync(0xffffffffu, go, 0)) {
                         ok = false;
                         break;
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(&bar->kv_full[st], nmine * a.block_size * 128);
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&bar->kv_full[st], vbytes + (i + 1 < n_tiles ? kbytes : 0));
                     __syncwarp();
-                    if (mine)
-                        tma_load_3d(sbase + OFF_KV + st * STAGE_BYTES + tt * KV_BYTES + c * KBOX +
-                                        blk * a.block_size * 128,
-                                    map, &bar->kv_full[st], 0, kvh * 2 + c, row);
+                    if (mine) tma_load_3d(dst0 + st * STAGE_BYTES, map, &bar->kv_full[st], 0, kvh * 2 + c, row);
                 }
             }
         } else {

@@ -77,12 +77,15 @@ def test_paged_invariant_to_block_placement():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("missing", [2, 8])
-def test_paged_missing_block_flags_and_zeroes(missing):
-    """A needed -1 entry of request 0: block 2 (positions 32..47, in the
-    first key tile, loaded before the block-wide barrier) or block 8
-    (positions 128..143, in the third tile, loaded by the ring loop)."""
-    c = make_varlen(4, [50, 60], [100, 20], 8, 2, 128, 16)
+@pytest.mark.parametrize("bs,missing", [(16, 2), (16, 8), (8, 3), (8, 17), (64, 0), (64, 2)])
+def test_paged_missing_block_flags_and_zeroes(bs, missing):
+    """A needed -1 entry of request 0 (150 keys): a block of the first key
+    tile, whose boxes go out before the block-wide barrier (bs=16 block 2,
+    bs=8 block 3, bs=64 block 0), or of the third tile, loaded by the ring
+    loop (bs=16 block 8, bs=8 block 17, bs=64 block 2).  Blocks of 8 and 16
+    keys split a tile's boxes over three loader warps, blocks of 64 over
+    two."""
+    c = make_varlen(4, [50, 60], [100, 20], 8, 2, 128, bs)
     c.block_table[0, missing] = -1
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     t = lambda x: x.to("cuda")
