@@ -15,7 +15,7 @@
 // over the head groups so the CTAs of one GQA group run side by side.  Tiles
 // are issued from the last (most keys under the causal mask) to the first.
 //
-// Warp roles (192 threads, 224 for paged keys; two CTAs share an SM, 96 KB
+// Warp roles (192 threads, 256 for paged keys; two CTAs share an SM, 103 KB
 // of shared memory and 256 TMEM columns each, so one CTA's softmax overlaps
 // the other's MMAs):
 //   warps 0-3  softmax: thread r owns query row r of the tile, which is TMEM
@@ -33,7 +33,7 @@
 //              stage i % 2 holds {V_(i-1), K_(i+1)} as a single TMA transaction
 //              (see NSTAGE below).  Paged keys: the same ring, but a tile is
 //              one box per pool block and 64-dim half, and warps 4, 6 and 7
-//              (6 only, for blocks of 32 or 64 keys) share each transaction's
+//              (4 and 6 for blocks of 32 or 64 keys) share each transaction's
 //              boxes, one box per lane.
 //   warp 5     TMEM allocator and MMA issuer (one thread): S_j = Q K_j^T into
 //              one of two TMEM S buffers (M=128, N=64, K=16 per instruction,
